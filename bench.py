@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the five-point Jacobi solver for implicit 2-D diffusion.
+
+One bench step = one full run of the method on one synthetic workload: u⁰
+reset, then ten backward-Euler time steps (fused right-hand side, Jacobi
+sweeps of the chosen strategy, residual every check interval, host stop
+decision), timed with CUDA events on the solver's stream, checks included
+("Synchronous vs block-async Jacobi on one RTX 5050", sections 01-03).
+
+Default workload: N = 2048 (ring included), r = 10, Gaussian source
+σ = N/16, amplitude 100, 10 time steps, tol 1e-5, M = 8; strategies SYNC and
+EXACT_TEMPORAL_BLOCKED with D = 2, 4, 8. `value` is the GLUP/s (interior
+points × sweeps ÷ time) of the fastest strategy; every strategy's figures
+are under "strategies". All strategies perform the same sweeps (exact
+temporal blocking is bit-identical to SYNC), so their GLUP/s compare
+time-to-solution directly.
+
+Usage:
+  python bench.py [--steps K] [--warmup W] [--workload NAME]
+                  [--strategies sync,etb2,etb4,etb8] [--impl ours|reference]
+Multi-GPU (torchrun, one rank per GPU): independent replicas of the same
+solve, no data exchange; value = all ranks' lattice updates ÷ max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from temporal_blocked_jacobi_gb300 import problem as P  # noqa: E402
+
+METRIC = "Jacobi GLUP/s, HBM GB/s vs peak, 10-step time-to-solution per strategy"
+UNIT = "GLUP/s"
+
+WORKLOADS = {
+    # name: (N, r, source, default strategies)
+    "n512_r1_point": (512, 1.0, "point", "sync"),
+    "n2048_r10_gauss": (2048, 10.0, "gauss", "sync,etb2,etb4,etb8"),
+    "n8192_r100_gauss": (8192, 100.0, "gauss", "sync,etb4,etb8,etb16"),
+    "n18432_r10_point": (18432, 10.0, "point", "sync,etb8,ba8"),
+    "n4096_r1_gauss": (4096, 1.0, "gauss", "sync,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16"),
+    "n4096_r10_gauss": (4096, 10.0, "gauss", "sync,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16"),
+    "n4096_r100_gauss": (4096, 100.0, "gauss", "sync,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16"),
+}
+DEFAULT_WORKLOAD = "n2048_r10_gauss"
+TIME_STEPS = 10
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def parse_strategy(tok: str):
+    """'sync' | 'etbD' | 'baD' | 'baD@TXxTY' -> kwargs for jacobi.Solver."""
+    tok = tok.strip()
+    tile = (0, 0)
+    if "@" in tok:
+        tok, t = tok.split("@")
+        tx, ty = t.lower().split("x")
+        tile = (int(tx), int(ty))
+    if tok == "sync":
+        return dict(strategy="sync", depth=1, tile=tile)
+    for prefix, name in (("etb", "etb"), ("ba", "ba")):
+        if tok.startswith(prefix):
+            return dict(strategy=name, depth=int(tok[len(prefix):]), tile=tile)
+    raise ValueError(f"unknown strategy {tok!r}")
+
+
+def sweeps_per_launch(kw):
+    return 1 if kw["strategy"] == "sync" else kw["depth"]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Multi-process plumbing (replicas): max of the elapsed time and sum of the
+# work over ranks. Works with any torch.distributed backend.
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_units: float, local_seconds: float, device=None):
+    """(sum of units over ranks, max of seconds over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_units, local_seconds
+    t = torch.tensor([local_units], dtype=torch.float64, device=device)
+    s = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(t.item()), float(s.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for name, flag in zip(names, flags[1:]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        sm = [r[0] for r in rows]
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    from temporal_blocked_jacobi_gb300 import jacobi
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    n, r, source, default_strats = WORKLOADS[args.workload]
+    strategies = [s for s in (args.strategies or default_strats).split(",") if s]
+    ld = P.padded_ld(n)
+    interior = (n - 2) ** 2
+
+    u0_host = P.initial_field(n, ld)
+    g_host = P.source_term(n, ld, source)
+    stream = torch.cuda.Stream(dev)
+    u0 = torch.from_numpy(u0_host).to(dev)
+    g = torch.from_numpy(g_host).to(dev)
+    u, u_alt, b = jacobi.allocate(n, ld, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    results = {}
+    solvers = {}
+    with torch.cuda.stream(stream):
+        for tok in strategies:
+            kw = parse_strategy(tok)
+            u.copy_(u0)
+            solvers[tok] = jacobi.Solver(u, u_alt, b, r, stream=stream, **kw)
+
+        def one_step(tok):
+            """Reset u⁰ (setup, untimed) and run the ten time steps (timed)."""
+            s = solvers[tok]
+            flush.fill_(1.0)  # evict the working set from L2
+            u.copy_(u0)
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            l0 = s.launch_count
+            start.record(stream)
+            counts = s.run(g, TIME_STEPS)
+            end.record(stream)
+            end.synchronize()
+            return start.elapsed_time(end), counts, s.launch_count - l0
+
+        # warm-up (also checks that every strategy reaches the same answer)
+        for tok in strategies:
+            for _ in range(args.warmup):
+                one_step(tok)
+
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.perf_counter()
+        with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+            for tok in strategies:
+                times, launches, counts = [], 0, None
+                for _ in range(args.steps):
+                    ms, counts, nl = one_step(tok)
+                    times.append(ms)
+                    launches += nl
+                sweeps = sum(counts)
+                ms_med = statistics.median(times)
+                results[tok] = dict(
+                    sweeps=sweeps, sweeps_per_step=counts,
+                    ms_per_solve_median=ms_med, ms_per_solve_mean=sum(times) / len(times),
+                    ms_per_solve_all=[round(t, 3) for t in times],
+                    glups=interior * sweeps / (ms_med * 1e-3) / 1e9,
+                    sync_equiv_gbs=12.0 * interior * sweeps / (ms_med * 1e-3) / 1e9,
+                    alg_gbs=12.0 * interior * sweeps / sweeps_per_launch(parse_strategy(tok))
+                    / (ms_med * 1e-3) / 1e9,
+                    launches=launches, total_ms=sum(times))
+        torch.cuda.synchronize(dev)
+        barrier()
+        wall = time.perf_counter() - t_wall0
+
+    # headline: fastest strategy
+    best = max(results, key=lambda t: results[t]["glups"])
+    base = results.get("sync")
+    for tok, res in results.items():
+        if base:
+            res["speedup_vs_sync"] = base["ms_per_solve_median"] / res["ms_per_solve_median"]
+            res["sweep_ratio_s"] = res["sweeps"] / base["sweeps"]
+            # cost per sweep relative to a synchronous sweep: S = 1/(c*s)
+            res["cost_per_sweep_c"] = 1.0 / (res["speedup_vs_sync"] * res["sweep_ratio_s"])
+    total_ms = sum(res["total_ms"] for res in results.values())
+    total_lups = sum(interior * res["sweeps"] * args.steps for res in results.values())
+    lups_all, seconds_max = aggregate(float(interior * results[best]["sweeps"] * args.steps),
+                                      results[best]["total_ms"] * 1e-3,
+                                      device=dev if world > 1 else None)
+    value = lups_all / seconds_max / 1e9
+
+    # --- dominant kernel: the headline strategy's sweep kernel, timed alone
+    roof = kernel_roofline(solvers[best], best, u, u0, stream, interior, args)
+
+    # --- end to end through the public API with host buffers
+    e2e = end_to_end(solvers[best], u, g, u0_host, g_host, stream, interior, args)
+
+    for s in solvers.values():
+        s.close()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": results[best]["ms_per_solve_median"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "n": n, "r": r, "source": source,
+                   "interior_points": interior, "time_steps": TIME_STEPS,
+                   "tol": 1e-5, "check_every": 8, "strategy": best,
+                   "strategies_timed": strategies,
+                   "l2": "flushed (512 MiB write) before every timed solve",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "e2e": e2e,
+        "gpu_launches": sum(res["launches"] for res in results.values()),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall, "device_ms_all_strategies": total_ms,
+        "lups_all_strategies": total_lups,
+        "strategies": results,
+    }
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def kernel_roofline(solver, tok, u, u0, stream, interior, args):
+    """Average duration of the strategy's sweep kernel, launched back to back
+    on the solver's stream (no checks), against the HBM roofline with the
+    algorithmic 12 B per interior point per launch."""
+    import torch
+    kw = parse_strategy(tok)
+    per = sweeps_per_launch(kw)
+    launches = max(8, 256 // per)
+    u.copy_(u0)
+    solver.sweeps(launches)  # warm
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    solver.sweeps(launches)
+    end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / launches
+    alg_bytes = 12.0 * interior  # read u, read b, write u' once per launch
+    peak, how = measured_peaks()
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    traffic = load_traffic(tok, args.workload)
+    return {"bound": "hbm", "kernel": kernel_name(tok), "achieved": achieved,
+            "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{how} (MEASURED_PEAKS.json hbm_gbs)" if how == "measured" else how,
+            "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
+            "launch_us": ms * 1e3, "sweeps_per_launch": per,
+            "lups_per_s": interior * per / (ms * 1e-3)}
+
+
+def kernel_name(tok):
+    kw = parse_strategy(tok)
+    if kw["strategy"] == "sync":
+        return "k_sweep_sync<16>"
+    return f"k_tiled<{kw['depth']},{'true' if kw['strategy'] == 'etb' else 'false'}>"
+
+
+def load_traffic(tok, workload):
+    """DRAM bytes per launch of this kernel from a committed ncu summary
+    (profiles/traffic.json), or None if it was not captured for the current
+    kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        return d.get(workload, {}).get(tok)
+    except (ValueError, OSError):
+        return None
+
+
+def end_to_end(solver, u, g, u0_host, g_host, stream, interior, args):
+    """Same metric through the public API with host buffers: each step copies
+    u⁰ and g from pinned host memory, runs the ten time steps and reads the
+    final field back."""
+    import torch
+    u0_pin = torch.from_numpy(u0_host).pin_memory()
+    g_pin = torch.from_numpy(g_host).pin_memory()
+    out_pin = torch.empty_like(u0_pin).pin_memory()
+    times, sweeps = [], 0
+    for it in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            u.copy_(u0_pin, non_blocking=True)
+            g.copy_(g_pin, non_blocking=True)
+            counts = solver.run(g, TIME_STEPS)
+            out_pin.copy_(u, non_blocking=True)
+        stream.synchronize()
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            times.append(dt)
+            sweeps = sum(counts)
+    med = statistics.median(times)
+    nbytes = u0_pin.numel() * 4
+    return {"value": interior * sweeps / med / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": nbytes,
+            "ms_per_step": med * 1e3, "clock": "host wall clock"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (test infrastructure, timed as a reported baseline)
+# ---------------------------------------------------------------------------
+def oracle_sample(n, r, source, sample_sweeps):
+    """Time the oracle (single-threaded C) on the first `sample_sweeps`
+    sweeps of time step 1 of the workload, residual checks included."""
+    import oracle
+    u0 = P.initial_field(n)
+    g = P.source_term(n, kind=source)
+    b = oracle.rhs(u0, g)
+    u = u0.copy()
+    oracle.solve_step(u, b, r, max_sweeps=8)  # warm the library and caches
+    u = u0.copy()
+    t0 = time.perf_counter()
+    k, _, _ = oracle.solve_step(u, b, r, max_sweeps=sample_sweeps)
+    dt = time.perf_counter() - t0
+    done = sample_sweeps if k < 0 else k
+    return (n - 2) ** 2 * done / dt / 1e9, dt, done
+
+
+def cpu_baseline(args):
+    n, r, source, _ = WORKLOADS[args.workload]
+    sweeps = args.cpu_sample_sweeps or max(8, int(8 * round(2.5e9 / (n - 2) ** 2 / 8)))
+    glups, dt, done = oracle_sample(n, r, source, sweeps)
+    return {"value": glups, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {done} sweeps of time step 1 (checks every 8), "
+                      f"single-threaded C oracle, {dt:.1f} s",
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    n, r, source, _ = WORKLOADS[args.workload]
+    sweeps = args.cpu_sample_sweeps or max(8, int(8 * round(1.0e9 / (n - 2) ** 2 / 8)))
+    oracle_sample(n, r, source, 8)  # warm-up outside the count
+    for _ in range(args.warmup):
+        oracle_sample(n, r, source, sweeps)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, dt, done = oracle_sample(n, r, source, sweeps)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "n": n, "r": r, "source": source,
+                       "strategy": "sync (oracle)", "parallelism": "single host core"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"first {sweeps} sweeps of time step 1 per bench step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--strategies", default=None,
+                    help="comma list: sync, etbD, baD, baD@TXxTY (default per workload)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-sweeps", type=int, default=0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

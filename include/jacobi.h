@@ -1,0 +1,178 @@
+/*
+ * jacobi.h -- C ABI of the GB300 (sm_103a) five-point Jacobi solver for
+ * implicit 2-D diffusion.
+ *
+ * The method is the one of "Synchronous vs block-async Jacobi on one
+ * RTX 5050" (stencil-jacobian.vercel.app):
+ *   section 01 "The problem": du/dt = alpha Lap u + f on an N x N unit square,
+ *     backward Euler; each step solves (1+4r) u_ij - r (uN+uS+uE+uW) = b_ij,
+ *     r = alpha dt / h^2, top boundary 100, the others 0, float32; a step
+ *     converges when ||b - Au||inf / ||b||inf < 1e-5, checked every M = 8
+ *     sweeps, the residual taken in a cancellation-free difference form;
+ *   section 02 "Method": the synchronous sweep, the fused right-hand side
+ *     b = u^n + dt f, the block-asynchronous kernel (tiles swept D times
+ *     against frozen one-cell halos) and exact temporal blocking (a D-deep
+ *     halo, shrinking valid region, bit-identical to D synchronous sweeps).
+ *
+ * Grid layout (all buffers): N x N float32 cells INCLUDING the Dirichlet ring,
+ * row-major with row pitch `ld` floats; cell (i, j) -- row i, i = 0 the top,
+ * column j -- lives at ptr[i * ld + j]. Requirements: N >= 3, ld >= N,
+ * ld % 4 == 0 (16-byte rows), every base pointer 16-byte aligned. Columns
+ * N..ld-1 are padding and are never read into a result or written.
+ *
+ * Arithmetic: every kernel evaluates
+ *   J(u)_ij = ((uW + uE) + (uN + uS)) * r  added to b_ij, divided by d,
+ *   d = 1 + 4r,
+ * as float32 round-to-nearest operations in exactly that order, with no
+ * fused multiply-add and with subnormals kept.
+ *
+ * Errors: every entry point returns a status (0 or a negative
+ * jacobi_status_t); none aborts or traps. Device-side waits are bounded and
+ * report JACOBI_ERR_CUDA through the handle when they give up.
+ *
+ * Threading: a handle is bound to one CUDA stream and must be used from one
+ * host thread at a time. All work is enqueued on that stream.
+ */
+#ifndef TEMPORAL_BLOCKED_JACOBI_GB300_JACOBI_H
+#define TEMPORAL_BLOCKED_JACOBI_GB300_JACOBI_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Strategies of section 02 "Method". */
+typedef enum {
+    JACOBI_SYNC = 0,                   /* one launch per sweep, ping-pong buffers */
+    JACOBI_EXACT_TEMPORAL_BLOCKED = 1, /* D sweeps per launch, bit-identical to SYNC */
+    JACOBI_BLOCK_ASYNC = 2             /* D in-tile sweeps per launch, frozen halos */
+} jacobi_strategy_t;
+
+typedef enum {
+    JACOBI_OK = 0,
+    JACOBI_ERR_INVALID_ARG = -1,  /* bad size, pitch, alignment, pointer or config */
+    JACOBI_ERR_CUDA = -2,         /* a CUDA call failed or a device wait gave up */
+    JACOBI_ERR_NOT_CONVERGED = -3,/* max_sweeps reached; u holds the last iterate */
+    JACOBI_ERR_NONFINITE = -4,    /* a residual norm is NaN or Inf */
+    JACOBI_ERR_UNSUPPORTED = -5   /* valid but not provided (e.g. tile too large) */
+} jacobi_status_t;
+
+/* How the convergence loop is driven. */
+typedef enum {
+    /* One CUDA graph per check interval; its last node copies (rmax, bmax)
+     * to pinned host memory and the host makes the stop/continue decision,
+     * as in section 02 where the reduction's two norms go back to the host. */
+    JACOBI_CONTROL_HOST = 0,
+    /* The check interval runs inside a device-side conditional WHILE graph
+     * node: the residual kernel sets the loop condition itself, so a whole
+     * time step is one graph launch and one host synchronisation. Same
+     * iterates, same sweep counts as JACOBI_CONTROL_HOST. */
+    JACOBI_CONTROL_DEVICE = 1
+} jacobi_control_t;
+
+typedef struct {
+    int strategy;         /* jacobi_strategy_t */
+    int depth;            /* D: SYNC 1; EXACT_TEMPORAL_BLOCKED 2,4,8,16; BLOCK_ASYNC 1,2,4,8,16 */
+    int tile_x, tile_y;   /* tile shape in cells; 0 = library default for the strategy.
+                             tile_x a multiple of 4 for both tiled strategies;
+                             BLOCK_ASYNC default 32 x 8 (section 02) */
+    int check_every;      /* M: residual checked every lcm(M, sweeps per launch) sweeps; default 8 */
+    double tol;           /* stop when rmax < tol * bmax (or rmax == 0); default 1e-5 */
+    long long max_sweeps; /* give up (JACOBI_ERR_NOT_CONVERGED) at this many sweeps; default 1<<22 */
+    int control;          /* jacobi_control_t; default JACOBI_CONTROL_HOST */
+    int reserved[3];      /* must be 0 */
+} jacobi_config_t;
+
+typedef struct jacobi_handle jacobi_handle_t;
+
+/* Fill *cfg with the defaults (SYNC, D 1, M 8, tol 1e-5, 1<<22 sweeps). */
+int jacobi_config_default(jacobi_config_t *cfg);
+
+/*
+ * Create a solver over caller-owned device buffers.
+ *   n, ld      grid side (ring included) and row pitch, see "Grid layout".
+ *   r          alpha dt / h^2 (section 01), finite and >= 0.
+ *   cfg        strategy and control; NULL = defaults.
+ *   u          N*ld floats: on entry u^n with its ring filled; the solution
+ *              of each step is left here.
+ *   u_alt      N*ld floats of scratch for ping-pong; its ring is overwritten
+ *              with u's ring here and never written again.
+ *   b          N*ld floats that receive the right-hand side (interior only).
+ *   cuda_stream a cudaStream_t (NULL = the legacy default stream).
+ * The caller keeps ownership of u, u_alt, b and must keep them alive and
+ * unmoved until jacobi_destroy. The handle owns its graphs, tensor maps,
+ * reduction scratch and pinned host words. On failure *out is NULL.
+ */
+int jacobi_create(jacobi_handle_t **out, int n, long long ld, float r,
+                  const jacobi_config_t *cfg, float *u, float *u_alt,
+                  float *b, void *cuda_stream);
+
+/*
+ * Fused right-hand side (section 02: u^n + dt f is formed once per time
+ * step instead of inside every sweep): b_ij = u_ij + g_ij on the interior,
+ * one float32 add per cell. g is a device buffer in the grid layout (g = dt f).
+ * Asynchronous on the handle's stream.
+ */
+int jacobi_rhs(jacobi_handle_t *h, const float *g);
+
+/*
+ * Solve one backward-Euler step from the warm start u = u^n (section 01:
+ * u^n stays fixed inside b while the iterate changes), using b from jacobi_rhs: launches of
+ * the configured strategy until the stopping rule holds at a check.
+ * Returns the number of sweeps (>= 0, a multiple of the check interval;
+ * for BLOCK_ASYNC launches x D) or a negative jacobi_status_t. On return
+ * (success or NOT_CONVERGED / NONFINITE) u holds the last checked iterate.
+ * Synchronises the stream.
+ */
+long long jacobi_solve_step(jacobi_handle_t *h);
+
+/*
+ * Run `launches` launches of the configured strategy on u with no residual
+ * check (for kernel-level tests and timing). Returns the sweeps performed
+ * (launches x sweeps per launch) or a negative status; the result is left
+ * in u. Asynchronous.
+ */
+long long jacobi_sweeps(jacobi_handle_t *h, long long launches);
+
+/*
+ * Residual norms of the current u (section 01): rmax = max over the
+ * interior of d |J(u) - u| (the difference form of |b - Au|), bmax = the
+ * max-norm of the right-hand side of the system in the unknowns,
+ * |b_ij + r (sum of the cell's Dirichlet-ring neighbours)|. NaN propagates
+ * into the norm. Host pointers; synchronises the stream.
+ */
+int jacobi_residual(jacobi_handle_t *h, float *rmax, float *bmax);
+
+/*
+ * Change strategy, depth, tile, tolerance or control between steps
+ * (section 02: D is a launch parameter, so switching it costs nothing).
+ * Rebuilds the handle's graphs. u must hold the current iterate.
+ */
+int jacobi_set_strategy(jacobi_handle_t *h, const jacobi_config_t *cfg);
+
+/*
+ * The time-step loop (section 01: a run is ten successive time steps): for each of
+ * `steps` steps, jacobi_rhs(g) then jacobi_solve_step; u^{n+1} replaces u^n
+ * in u. sweeps_per_step (host, `steps` entries, may be NULL) receives each
+ * step's count. Returns the total sweep count or the first negative status.
+ */
+long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
+                     long long *sweeps_per_step);
+
+/* Number of kernels this handle has launched so far (graph nodes included). */
+long long jacobi_launch_count(const jacobi_handle_t *h);
+
+/* Release library-owned state only; the caller's buffers are untouched. */
+void jacobi_destroy(jacobi_handle_t *h);
+
+/* Text of the last error on this handle ("" if none); valid until the next
+ * call on the handle. For h == NULL, the last jacobi_create failure. */
+const char *jacobi_last_error(const jacobi_handle_t *h);
+
+/* Static name of a status code. */
+const char *jacobi_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TEMPORAL_BLOCKED_JACOBI_GB300_JACOBI_H */

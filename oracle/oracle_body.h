@@ -46,8 +46,8 @@ static REAL FN(diag)(REAL r) {
     return (REAL)1 + four_r;
 }
 
-/* Fused right-hand side, once per time step (section 02: "uⁿ + Δt·f
- * computed once per step"): b = u + g on the interior. The ring of b is left
+/* Fused right-hand side, formed once per time step (section 02):
+ * b = u + g on the interior. The ring of b is left
  * untouched (it is never read). */
 void FN(oracle_rhs)(int n, long long ld, const REAL *u, const REAL *g,
                     REAL *b) {
@@ -77,14 +77,14 @@ static int FN(on_ring)(int n, int i, int j) {
 }
 
 /*
- * Residual norms in the difference form (section 01: "computed in a
- * difference form that avoids float32 cancellation"). Per interior cell
+ * Residual norms in the difference form of section 01 (chosen there because
+ * forming b - Au directly loses digits to float32 cancellation). Per cell
  *   e_ij = d * |J(u)_ij - u_ij|,
  * which equals |b - A u|_ij in exact arithmetic because
  * d (J(u) - u) = b + r s - d u. J is evaluated exactly as in the sweep.
  *
  * ||b||inf is the norm of the right-hand side of the linear system in the
- * unknowns (section 01, "Each backward-Euler step solves a linear system"):
+ * unknowns (section 01: every backward-Euler step is a linear solve):
  * the Dirichlet values are known, so they move to the right-hand side, and
  *   bI_ij = b_ij + r * q_ij,  q_ij = (qW + qE) + (qN + qS),
  * where qX is the neighbour's value when that neighbour is a ring cell and 0
@@ -200,8 +200,8 @@ static long long FN(gcd)(long long a, long long b) {
 }
 
 /*
- * Solve one backward-Euler step from the warm start u (= uⁿ, section 01,
- * "Jacobi update with uⁿ held fixed"): repeat launches of the chosen
+ * Solve one backward-Euler step from the warm start u (= uⁿ; section 01
+ * keeps uⁿ fixed inside b while the iterate moves): repeat launches of the chosen
  * strategy, and after every check interval evaluate the residual and stop
  * when the stopping rule holds.
  *   depth == 0 : synchronous sweeps, one sweep per launch.
@@ -252,8 +252,8 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
 }
 
 /*
- * Ten (or `steps`) backward-Euler steps from u = u⁰ (section 01: "Each run
- * solves ten consecutive time steps"): b = u + g, then solve to the stopping
+ * Ten (or `steps`) backward-Euler steps from u = u⁰ (section 01: a run is
+ * ten successive time steps): b = u + g, then solve to the stopping
  * rule warm-started from uⁿ; the converged iterate becomes uⁿ⁺¹ in place.
  * sweeps[s] receives each step's count (or its negative status, after which
  * the run stops). Returns 0, or the first negative status.

@@ -1,0 +1,495 @@
+// C ABI of the solver (declared in include/jacobi.h): argument checking,
+// TMA tensor maps, one CUDA graph per check interval, and the convergence
+// loop of "Synchronous vs block-async Jacobi on one RTX 5050", sections
+// 01-02.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/jacobi.h"
+#include "jacobi_kernels.cuh"
+
+using namespace tbj;
+
+struct jacobi_handle {
+    GridDesc g;
+    jacobi_config_t cfg;
+    float *u = nullptr, *u_alt = nullptr, *b = nullptr;  // caller-owned
+    cudaStream_t stream = nullptr;   // caller's stream: all work goes here
+    cudaStream_t capture = nullptr;  // private stream used to record graphs
+
+    // Library-owned device scratch.
+    float *partials = nullptr;     // 2 words per residual block
+    ResidualOut *dev_out = nullptr;
+    ResidualOut *host_out = nullptr;  // pinned
+
+    // Tiled strategies.
+    TileConf tc{};
+    CUtensorMap map_u{}, map_alt{}, map_b{};
+
+    // Sweeps per launch, launches per check, sweeps per check.
+    int per_launch = 1;
+    long long launches_per_check = 8;
+    long long interval = 8;
+
+    // Graph for a check interval starting from u (index 0) and from u_alt
+    // (index 1; only when launches_per_check is odd).
+    cudaGraphExec_t batch[2] = {nullptr, nullptr};
+    int cur = 0;  // 0: the iterate is in u; 1: in u_alt
+
+    long long launches = 0;  // kernels launched so far
+    char err[512] = {0};
+};
+
+namespace {
+
+thread_local char g_create_err[512];
+
+int fail(jacobi_handle_t *h, int status, const char *fmt, ...) {
+    char *dst = h ? h->err : g_create_err;
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(dst, 512, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+#define TBJ_CUDA(h, call)                                                     \
+    do {                                                                      \
+        cudaError_t e_ = (call);                                              \
+        if (e_ != cudaSuccess)                                                \
+            return fail((h), JACOBI_ERR_CUDA, "%s: %s", #call,                \
+                        cudaGetErrorString(e_));                              \
+    } while (0)
+
+bool aligned16(const void *p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool is_device_pointer(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p,
+                                             12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int make_map(jacobi_handle_t *h, CUtensorMap *map, const float *ptr) {
+    auto fn = encode_fn();
+    if (!fn) return fail(h, JACOBI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {(cuuint64_t)h->g.n, (cuuint64_t)h->g.n};
+    const cuuint64_t strides[1] = {(cuuint64_t)h->g.ld * sizeof(float)};
+    const cuuint32_t box[2] = {(cuuint32_t)h->tc.box_x,
+                               (cuuint32_t)h->tc.box_y};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    const_cast<float *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(h, JACOBI_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)",
+                    (int)r);
+    return JACOBI_OK;
+}
+
+long long gcd_ll(long long a, long long b) {
+    while (b) {
+        long long t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
+    for (int k = 0; k < 3; ++k)
+        if (c.reserved[k])
+            return fail(h, JACOBI_ERR_INVALID_ARG, "reserved fields must be 0");
+    if (c.check_every < 1)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "check_every must be >= 1");
+    if (!(c.tol >= 0.0) || !std::isfinite(c.tol))
+        return fail(h, JACOBI_ERR_INVALID_ARG, "tol must be finite and >= 0");
+    if (c.max_sweeps < 1)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "max_sweeps must be >= 1");
+    if (c.control != JACOBI_CONTROL_HOST && c.control != JACOBI_CONTROL_DEVICE)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "unknown control %d", c.control);
+    if (c.control == JACOBI_CONTROL_DEVICE)
+        return fail(h, JACOBI_ERR_UNSUPPORTED,
+                    "device-side control is not available in this build");
+    switch (c.strategy) {
+        case JACOBI_SYNC:
+            if (c.depth != 1)
+                return fail(h, JACOBI_ERR_INVALID_ARG, "SYNC takes depth 1");
+            break;
+        case JACOBI_EXACT_TEMPORAL_BLOCKED:
+            if (c.depth != 2 && c.depth != 4 && c.depth != 8 && c.depth != 16)
+                return fail(h, JACOBI_ERR_INVALID_ARG,
+                            "EXACT_TEMPORAL_BLOCKED takes depth 2, 4, 8 or 16");
+            break;
+        case JACOBI_BLOCK_ASYNC:
+            if (c.depth != 1 && c.depth != 2 && c.depth != 4 && c.depth != 8 &&
+                c.depth != 16)
+                return fail(h, JACOBI_ERR_INVALID_ARG,
+                            "BLOCK_ASYNC takes depth 1, 2, 4, 8 or 16");
+            break;
+        default:
+            return fail(h, JACOBI_ERR_INVALID_ARG, "unknown strategy %d",
+                        c.strategy);
+    }
+    if (c.tile_x < 0 || c.tile_y < 0)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "tile sizes must be >= 0");
+    return JACOBI_OK;
+}
+
+// Enqueue one launch of the configured strategy: src -> dst.
+cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
+                           cudaStream_t s) {
+    const float *src = src_is_alt ? h->u_alt : h->u;
+    float *dst = src_is_alt ? h->u : h->u_alt;
+    const CUtensorMap *map_src = src_is_alt ? &h->map_alt : &h->map_u;
+    switch (h->cfg.strategy) {
+        case JACOBI_SYNC:
+            return launch_sweep_sync(h->g, src, h->b, dst, s);
+        case JACOBI_EXACT_TEMPORAL_BLOCKED:
+            return launch_sweep_etb(h->g, h->tc, map_src, &h->map_b, dst,
+                                    h->dev_out, s);
+        default:
+            return launch_sweep_ba(h->g, h->tc, map_src, &h->map_b, dst,
+                                   h->dev_out, s);
+    }
+}
+
+void destroy_graphs(jacobi_handle_t *h) {
+    for (auto &e : h->batch) {
+        if (e) cudaGraphExecDestroy(e);
+        e = nullptr;
+    }
+}
+
+// Record the check interval starting from buffer `start` (0 = u, 1 = u_alt):
+// launches_per_check launches, the residual of the resulting iterate, and a
+// copy of the result block to pinned host memory.
+int record_batch(jacobi_handle_t *h, int start, cudaGraphExec_t *exec) {
+    TBJ_CUDA(h, cudaStreamBeginCapture(h->capture,
+                                       cudaStreamCaptureModeThreadLocal));
+    int src = start;
+    cudaError_t e = cudaSuccess;
+    for (long long l = 0; l < h->launches_per_check && e == cudaSuccess; ++l) {
+        e = enqueue_launch(h, src, h->capture);
+        src ^= 1;
+    }
+    if (e == cudaSuccess)
+        e = launch_residual(h->g, src ? h->u_alt : h->u, h->b, h->partials,
+                            h->dev_out, 0, h->cfg.tol, h->capture);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(h->host_out, h->dev_out, sizeof(ResidualOut),
+                            cudaMemcpyDeviceToHost, h->capture);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e2 = cudaStreamEndCapture(h->capture, &graph);
+    if (e == cudaSuccess) e = e2;
+    if (e == cudaSuccess) e = cudaGraphInstantiate(exec, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess)
+        return fail(h, JACOBI_ERR_CUDA, "recording the check graph: %s",
+                    cudaGetErrorString(e));
+    return JACOBI_OK;
+}
+
+// Apply a (validated) configuration: tiles, tensor maps, graphs.
+int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
+    destroy_graphs(h);
+    h->cfg = c;
+    int rc = 0;
+    if (c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED)
+        rc = etb_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc);
+    else if (c.strategy == JACOBI_BLOCK_ASYNC)
+        rc = ba_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc);
+    if (rc == -1)
+        return fail(h, JACOBI_ERR_INVALID_ARG,
+                    "tile %dx%d not valid for this strategy (tile_x must be a "
+                    "multiple of 4)",
+                    c.tile_x, c.tile_y);
+    if (rc)
+        return fail(h, JACOBI_ERR_UNSUPPORTED,
+                    "tile %dx%d with depth %d needs a TMA box over 256 or more "
+                    "shared memory than a block can have",
+                    c.tile_x, c.tile_y, c.depth);
+    if (c.strategy != JACOBI_SYNC) {
+        if ((rc = make_map(h, &h->map_u, h->u)) ||
+            (rc = make_map(h, &h->map_alt, h->u_alt)) ||
+            (rc = make_map(h, &h->map_b, h->b)))
+            return rc;
+        TBJ_CUDA(h, c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED
+                        ? prepare_sweep_etb(h->tc)
+                        : prepare_sweep_ba(h->tc));
+    }
+    h->per_launch = c.strategy == JACOBI_SYNC ? 1 : c.depth;
+    h->interval = (long long)c.check_every /
+                  gcd_ll(c.check_every, h->per_launch) * h->per_launch;
+    h->launches_per_check = h->interval / h->per_launch;
+    if ((rc = record_batch(h, 0, &h->batch[0]))) return rc;
+    if (h->launches_per_check % 2 == 1)
+        if ((rc = record_batch(h, 1, &h->batch[1]))) return rc;
+    return JACOBI_OK;
+}
+
+// Bring the iterate back into u if it sits in u_alt.
+int settle(jacobi_handle_t *h) {
+    if (h->cur == 1) {
+        TBJ_CUDA(h, launch_copy_interior(h->g, h->u_alt, h->u, h->stream));
+        h->launches += 1;
+        h->cur = 0;
+    }
+    return JACOBI_OK;
+}
+
+int check_device_status(jacobi_handle_t *h, unsigned err) {
+    if (err & ERR_TMA_TIMEOUT) {
+        // Clear the word so the handle stays usable, then report.
+        cudaMemsetAsync(&h->dev_out->err, 0, sizeof(unsigned), h->stream);
+        return fail(h, JACOBI_ERR_CUDA,
+                    "a TMA load did not complete within its wait limit");
+    }
+    return JACOBI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int jacobi_config_default(jacobi_config_t *cfg) {
+    if (!cfg) return JACOBI_ERR_INVALID_ARG;
+    std::memset(cfg, 0, sizeof(*cfg));
+    cfg->strategy = JACOBI_SYNC;
+    cfg->depth = 1;
+    cfg->check_every = 8;
+    cfg->tol = 1e-5;
+    cfg->max_sweeps = 1ll << 22;
+    cfg->control = JACOBI_CONTROL_HOST;
+    return JACOBI_OK;
+}
+
+int jacobi_create(jacobi_handle_t **out, int n, long long ld, float r,
+                  const jacobi_config_t *cfg, float *u, float *u_alt,
+                  float *b, void *cuda_stream) {
+    if (!out) return fail(nullptr, JACOBI_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    g_create_err[0] = 0;
+    if (n < 3) return fail(nullptr, JACOBI_ERR_INVALID_ARG, "n must be >= 3");
+    if (ld < n || ld % 4 != 0)
+        return fail(nullptr, JACOBI_ERR_INVALID_ARG,
+                    "ld must be >= n and a multiple of 4 (got %lld)", ld);
+    if (!std::isfinite(r) || r < 0.f)
+        return fail(nullptr, JACOBI_ERR_INVALID_ARG, "r must be finite and >= 0");
+    if (!u || !u_alt || !b || u == u_alt || u == b || u_alt == b)
+        return fail(nullptr, JACOBI_ERR_INVALID_ARG,
+                    "u, u_alt and b must be distinct non-NULL buffers");
+    if (!aligned16(u) || !aligned16(u_alt) || !aligned16(b))
+        return fail(nullptr, JACOBI_ERR_INVALID_ARG,
+                    "u, u_alt and b must be 16-byte aligned");
+    if (!is_device_pointer(u) || !is_device_pointer(u_alt) ||
+        !is_device_pointer(b))
+        return fail(nullptr, JACOBI_ERR_INVALID_ARG,
+                    "u, u_alt and b must be device memory");
+    jacobi_config_t c;
+    if (cfg)
+        c = *cfg;
+    else
+        jacobi_config_default(&c);
+    int rc = check_config(nullptr, c);
+    if (rc) return rc;
+
+    jacobi_handle_t *h = new (std::nothrow) jacobi_handle_t();
+    if (!h) return fail(nullptr, JACOBI_ERR_CUDA, "out of host memory");
+    h->g.n = n;
+    h->g.ld = ld;
+    h->g.r = r;
+    {
+        // d = fl(1 + fl(4 r)) in float32 (host code, -ffp-contract=off).
+        volatile float four_r = 4.0f * r;
+        h->g.d = 1.0f + four_r;
+    }
+    h->u = u;
+    h->u_alt = u_alt;
+    h->b = b;
+    h->stream = static_cast<cudaStream_t>(cuda_stream);
+    auto bail = [&](int status) {
+        std::snprintf(g_create_err, sizeof g_create_err, "%s", h->err);
+        jacobi_destroy(h);
+        return status;
+    };
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&h->capture, cudaStreamNonBlocking)) ||
+        (e = cudaMalloc(&h->partials,
+                        sizeof(float) * 2 * (size_t)residual_blocks(h->g))) ||
+        (e = cudaMalloc(&h->dev_out, sizeof(ResidualOut))) ||
+        (e = cudaMallocHost(&h->host_out, sizeof(ResidualOut))) ||
+        (e = cudaMemsetAsync(h->dev_out, 0, sizeof(ResidualOut), h->stream)) ||
+        // Both ping-pong buffers carry the same Dirichlet ring.
+        (e = cudaMemcpyAsync(u_alt, u, sizeof(float) * (size_t)n * (size_t)ld,
+                             cudaMemcpyDeviceToDevice, h->stream))) {
+        fail(h, JACOBI_ERR_CUDA, "allocating solver state: %s",
+             cudaGetErrorString(e));
+        return bail(JACOBI_ERR_CUDA);
+    }
+    std::memset(h->host_out, 0, sizeof(ResidualOut));
+    if ((rc = apply_config(h, c))) return bail(rc);
+    *out = h;
+    return JACOBI_OK;
+}
+
+int jacobi_rhs(jacobi_handle_t *h, const float *g) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (!g || !aligned16(g))
+        return fail(h, JACOBI_ERR_INVALID_ARG, "g must be a 16-byte aligned buffer");
+    int rc = settle(h);
+    if (rc) return rc;
+    TBJ_CUDA(h, launch_rhs(h->g, h->u, g, h->b, h->stream));
+    h->launches += 1;
+    return JACOBI_OK;
+}
+
+long long jacobi_solve_step(jacobi_handle_t *h) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    long long k = 0;
+    int status = JACOBI_OK;
+    for (;;) {
+        const int start = h->cur;
+        TBJ_CUDA(h, cudaGraphLaunch(h->batch[start], h->stream));
+        TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+        h->launches += h->launches_per_check + 1;
+        if (h->launches_per_check % 2 == 1) h->cur ^= 1;
+        k += h->interval;
+        const ResidualOut ro = *h->host_out;
+        if ((status = check_device_status(h, ro.err))) break;
+        const double rm = (double)ro.rmax, bm = (double)ro.bmax;
+        if (!std::isfinite(rm) || !std::isfinite(bm)) {
+            status = fail(h, JACOBI_ERR_NONFINITE,
+                          "residual norms not finite (rmax=%g, bmax=%g) after "
+                          "%lld sweeps",
+                          rm, bm, k);
+            break;
+        }
+        if (rm == 0.0 || rm < h->cfg.tol * bm) break;
+        if (k >= h->cfg.max_sweeps) {
+            status = fail(h, JACOBI_ERR_NOT_CONVERGED,
+                          "not converged after %lld sweeps (rho=%g)", k,
+                          bm > 0 ? rm / bm : rm);
+            break;
+        }
+    }
+    int rc = settle(h);
+    if (rc) return rc;
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    return status ? status : k;
+}
+
+long long jacobi_sweeps(jacobi_handle_t *h, long long launches) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (launches < 0)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "launches must be >= 0");
+    for (long long l = 0; l < launches; ++l) {
+        TBJ_CUDA(h, enqueue_launch(h, h->cur, h->stream));
+        h->cur ^= 1;
+        h->launches += 1;
+    }
+    int rc = settle(h);
+    if (rc) return rc;
+    return launches * h->per_launch;
+}
+
+int jacobi_residual(jacobi_handle_t *h, float *rmax, float *bmax) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (!rmax || !bmax)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "rmax and bmax must be non-NULL");
+    int rc = settle(h);
+    if (rc) return rc;
+    TBJ_CUDA(h, launch_residual(h->g, h->u, h->b, h->partials, h->dev_out, 0,
+                                h->cfg.tol, h->stream));
+    h->launches += 1;
+    TBJ_CUDA(h, cudaMemcpyAsync(h->host_out, h->dev_out, sizeof(ResidualOut),
+                                cudaMemcpyDeviceToHost, h->stream));
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    *rmax = h->host_out->rmax;
+    *bmax = h->host_out->bmax;
+    return check_device_status(h, h->host_out->err);
+}
+
+int jacobi_set_strategy(jacobi_handle_t *h, const jacobi_config_t *cfg) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (!cfg) return fail(h, JACOBI_ERR_INVALID_ARG, "cfg is NULL");
+    int rc = check_config(h, *cfg);
+    if (rc) return rc;
+    if ((rc = settle(h))) return rc;
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    return apply_config(h, *cfg);
+}
+
+long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
+                     long long *sweeps_per_step) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (steps < 0) return fail(h, JACOBI_ERR_INVALID_ARG, "steps must be >= 0");
+    long long total = 0;
+    for (int s = 0; s < steps; ++s) {
+        int rc = jacobi_rhs(h, g);
+        if (rc) return rc;
+        long long k = jacobi_solve_step(h);
+        if (sweeps_per_step) sweeps_per_step[s] = k;
+        if (k < 0) return k;
+        total += k;
+    }
+    return total;
+}
+
+long long jacobi_launch_count(const jacobi_handle_t *h) {
+    return h ? h->launches : 0;
+}
+
+void jacobi_destroy(jacobi_handle_t *h) {
+    if (!h) return;
+    if (h->stream || h->capture) cudaStreamSynchronize(h->stream);
+    destroy_graphs(h);
+    if (h->capture) cudaStreamDestroy(h->capture);
+    if (h->partials) cudaFree(h->partials);
+    if (h->dev_out) cudaFree(h->dev_out);
+    if (h->host_out) cudaFreeHost(h->host_out);
+    delete h;
+}
+
+const char *jacobi_last_error(const jacobi_handle_t *h) {
+    return h ? h->err : g_create_err;
+}
+
+const char *jacobi_status_string(int status) {
+    switch (status) {
+        case JACOBI_OK: return "JACOBI_OK";
+        case JACOBI_ERR_INVALID_ARG: return "JACOBI_ERR_INVALID_ARG";
+        case JACOBI_ERR_CUDA: return "JACOBI_ERR_CUDA";
+        case JACOBI_ERR_NOT_CONVERGED: return "JACOBI_ERR_NOT_CONVERGED";
+        case JACOBI_ERR_NONFINITE: return "JACOBI_ERR_NONFINITE";
+        case JACOBI_ERR_UNSUPPORTED: return "JACOBI_ERR_UNSUPPORTED";
+        default: return "JACOBI_STATUS_UNKNOWN";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,324 @@
+// Row-streaming kernels: fused right-hand side, synchronous sweep, residual
+// reduction and the interior copy.
+//
+// Layout of the work: a warp owns a strip 128 floats wide (32 lanes x one
+// float4 each) and ROWS consecutive grid rows. It walks down the strip
+// holding rows i-1, i and i+1 in registers, so every float of u is read from
+// memory once per strip (plus the two rows above and below it). The west and
+// east neighbours of a lane's four cells come from the adjacent lanes through
+// warp shuffles; only lanes 0 and 31 read one extra float per row. One sweep
+// therefore moves 4 B of u, 4 B of b and 4 B of u' per cell: the 12 B/cell
+// of "Synchronous vs block-async Jacobi on one RTX 5050", section 02.
+#include "jacobi_kernels.cuh"
+
+namespace tbj {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kWarps = 4;       // warps per block, stacked vertically
+constexpr int kSweepRows = 16;  // rows per warp in a sweep
+constexpr int kResidRows = 32;  // rows per warp in the residual
+
+__device__ __forceinline__ float4 ld4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ void st4(float *p, float4 v) {
+    *reinterpret_cast<float4 *>(p) = v;
+}
+
+// Store the cells of a float4 at column x0 that lie in [1, n-2].
+__device__ __forceinline__ void store_interior(float *row, int x0, int n,
+                                               float4 v) {
+    if (x0 >= 1 && x0 + 3 <= n - 2) {
+        st4(row + x0, v);
+    } else {
+        if (x0 + 0 >= 1 && x0 + 0 <= n - 2) row[x0 + 0] = v.x;
+        if (x0 + 1 >= 1 && x0 + 1 <= n - 2) row[x0 + 1] = v.y;
+        if (x0 + 2 >= 1 && x0 + 2 <= n - 2) row[x0 + 2] = v.z;
+        if (x0 + 3 >= 1 && x0 + 3 <= n - 2) row[x0 + 3] = v.w;
+    }
+}
+
+// One row's inputs for a lane: the centre float4 of u and the extra float
+// that lane 0 (west) or lane 31 (east) needs from beyond the warp's strip.
+struct RowIn {
+    float4 bot;   // u[i+1][x0..x0+3]
+    float4 bb;    // b[i][x0..x0+3]
+    float edge;   // lane 0: u[i][x0-1]; lane 31: u[i][x0+4]; others unused
+};
+
+__device__ __forceinline__ RowIn load_row(const float *__restrict__ u,
+                                          const float *__restrict__ b,
+                                          long long ld, int n, int i, int x0,
+                                          int lane, bool active) {
+    RowIn in;
+    in.bot = make_float4(0.f, 0.f, 0.f, 0.f);
+    in.bb = in.bot;
+    in.edge = 0.f;
+    if (active) {
+        const long long row = (long long)i * ld;
+        in.bot = ld4(u + row + ld + x0);
+        in.bb = ld4(b + row + x0);
+        if (lane == 0 && x0 > 0) in.edge = u[row + x0 - 1];
+        if (lane == 31 && x0 + 4 < n) in.edge = u[row + x0 + 4];
+    }
+    return in;
+}
+
+// ---------------------------------------------------------------------------
+// Synchronous sweep u -> out (section 02 "Synchronous"): every interior cell
+// gets J(u); the ring of out is never written.
+// ---------------------------------------------------------------------------
+template <int ROWS>
+__global__ void __launch_bounds__(32 * kWarps)
+k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
+             float *__restrict__ out, int n, long long ld, float r, float d) {
+    const int lane = threadIdx.x;
+    const int vx = blockIdx.x * 32 + lane;
+    const int x0 = vx * 4;
+    const bool active = x0 < n;
+    const int i0 = 1 + (blockIdx.y * kWarps + threadIdx.y) * ROWS;
+    if (i0 > n - 2) return;  // uniform across the warp
+    const int i1 = min(i0 + ROWS, n - 1);
+
+    float4 top = make_float4(0.f, 0.f, 0.f, 0.f), mid = top;
+    if (active) {
+        top = ld4(u + (long long)(i0 - 1) * ld + x0);
+        mid = ld4(u + (long long)i0 * ld + x0);
+    }
+    RowIn next = load_row(u, b, ld, n, i0, x0, lane, active);
+    for (int i = i0; i < i1; ++i) {
+        const RowIn cur = next;
+        if (i + 1 < i1) next = load_row(u, b, ld, n, i + 1, x0, lane, active);
+        float west = __shfl_up_sync(FULL, mid.w, 1);
+        float east = __shfl_down_sync(FULL, mid.x, 1);
+        if (lane == 0) west = cur.edge;
+        if (lane == 31) east = cur.edge;
+        float4 o;
+        o.x = jacobi_update(west, mid.y, top.x, cur.bot.x, cur.bb.x, r, d);
+        o.y = jacobi_update(mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, r, d);
+        o.z = jacobi_update(mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, r, d);
+        o.w = jacobi_update(mid.z, east, top.w, cur.bot.w, cur.bb.w, r, d);
+        if (active) store_interior(out + (long long)i * ld, x0, n, o);
+        top = mid;
+        mid = cur.bot;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Residual norms (section 01, difference form). Per interior cell:
+//   e  = d * |J(u) - u|
+//   bI = b + r * ((qW + qE) + (qN + qS)),  qX = neighbour value if it lies on
+//        the Dirichlet ring, else 0 (right-hand side of the system in the
+//        unknowns)
+// rmax = max e, bmax = max |bI|. Maxima are taken on the IEEE bit patterns
+// of non-negative floats, which order like the values and put NaN above
+// +Inf, so a NaN anywhere reaches the result. Each block writes its two
+// maxima to `partials`; the last block to finish reduces them, writes `out`
+// and re-arms the ticket.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned fbits(float x) {
+    return __float_as_uint(fabsf(x));
+}
+
+__device__ __forceinline__ void cell_norms(float c, float west, float east,
+                                           float north, float south, float bb,
+                                           int i, int x, int n, float r,
+                                           float d, unsigned &rm,
+                                           unsigned &bm) {
+    if (x < 1 || x > n - 2) return;
+    const float ju = jacobi_update(west, east, north, south, bb, r, d);
+    const float e = __fmul_rn(d, fabsf(__fsub_rn(ju, c)));
+    const float qw = (x - 1 == 0) ? west : 0.f;
+    const float qe = (x + 1 == n - 1) ? east : 0.f;
+    const float qn = (i - 1 == 0) ? north : 0.f;
+    const float qs = (i + 1 == n - 1) ? south : 0.f;
+    const float q = __fadd_rn(__fadd_rn(qw, qe), __fadd_rn(qn, qs));
+    const float bi = __fadd_rn(bb, __fmul_rn(r, q));
+    rm = max(rm, fbits(e));
+    bm = max(bm, fbits(bi));
+}
+
+__device__ __forceinline__ unsigned warp_max(unsigned v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+
+template <int ROWS>
+__global__ void __launch_bounds__(32 * kWarps)
+k_residual(const float *__restrict__ u, const float *__restrict__ b, int n,
+           long long ld, float r, float d, unsigned *__restrict__ partials,
+           ResidualOut *__restrict__ out) {
+    const int lane = threadIdx.x;
+    const int vx = blockIdx.x * 32 + lane;
+    const int x0 = vx * 4;
+    const bool active = x0 < n;
+    const int i0 = 1 + (blockIdx.y * kWarps + threadIdx.y) * ROWS;
+    const int i1 = min(i0 + ROWS, n - 1);
+    unsigned rm = 0u, bm = 0u;
+    if (i0 <= n - 2) {
+        float4 top = make_float4(0.f, 0.f, 0.f, 0.f), mid = top;
+        if (active) {
+            top = ld4(u + (long long)(i0 - 1) * ld + x0);
+            mid = ld4(u + (long long)i0 * ld + x0);
+        }
+        RowIn next = load_row(u, b, ld, n, i0, x0, lane, active);
+        for (int i = i0; i < i1; ++i) {
+            const RowIn cur = next;
+            if (i + 1 < i1) next = load_row(u, b, ld, n, i + 1, x0, lane, active);
+            float west = __shfl_up_sync(FULL, mid.w, 1);
+            float east = __shfl_down_sync(FULL, mid.x, 1);
+            if (lane == 0) west = cur.edge;
+            if (lane == 31) east = cur.edge;
+            if (active) {
+                cell_norms(mid.x, west, mid.y, top.x, cur.bot.x, cur.bb.x, i, x0 + 0, n, r, d, rm, bm);
+                cell_norms(mid.y, mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, i, x0 + 1, n, r, d, rm, bm);
+                cell_norms(mid.z, mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, i, x0 + 2, n, r, d, rm, bm);
+                cell_norms(mid.w, mid.z, east, top.w, cur.bot.w, cur.bb.w, i, x0 + 3, n, r, d, rm, bm);
+            }
+            top = mid;
+            mid = cur.bot;
+        }
+    }
+    rm = warp_max(rm);
+    bm = warp_max(bm);
+    __shared__ unsigned s_r[kWarps], s_b[kWarps];
+    __shared__ bool s_last;
+    if (lane == 0) {
+        s_r[threadIdx.y] = rm;
+        s_b[threadIdx.y] = bm;
+    }
+    __syncthreads();
+    const unsigned nblocks = gridDim.x * gridDim.y;
+    const unsigned bid = blockIdx.y * gridDim.x + blockIdx.x;
+    if (threadIdx.y == 0 && lane == 0) {
+        unsigned br = 0u, bbm = 0u;
+        for (int w = 0; w < kWarps; ++w) {
+            br = max(br, s_r[w]);
+            bbm = max(bbm, s_b[w]);
+        }
+        partials[2 * bid] = br;
+        partials[2 * bid + 1] = bbm;
+        __threadfence();
+        const unsigned t = atomicAdd(&out->ticket, 1u);
+        s_last = (t == nblocks - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    // Last block: reduce all partials.
+    __threadfence();
+    const int tid = threadIdx.y * 32 + lane;
+    rm = 0u;
+    bm = 0u;
+    const volatile unsigned *vp = partials;
+    for (unsigned k = tid; k < nblocks; k += 32 * kWarps) {
+        rm = max(rm, vp[2 * k]);
+        bm = max(bm, vp[2 * k + 1]);
+    }
+    rm = warp_max(rm);
+    bm = warp_max(bm);
+    __syncthreads();
+    if (lane == 0) {
+        s_r[threadIdx.y] = rm;
+        s_b[threadIdx.y] = bm;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned br = 0u, bbm = 0u;
+        for (int w = 0; w < kWarps; ++w) {
+            br = max(br, s_r[w]);
+            bbm = max(bbm, s_b[w]);
+        }
+        out->rmax = __uint_as_float(br);
+        out->bmax = __uint_as_float(bbm);
+        out->ticket = 0u;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fused right-hand side b = u + g and the interior copy dst = src: one float4
+// per thread, grid-stride over rows.
+// ---------------------------------------------------------------------------
+__global__ void k_rhs(const float *__restrict__ u, const float *__restrict__ g,
+                      float *__restrict__ b, int n, long long ld) {
+    const int x0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (x0 >= n) return;
+    for (int i = 1 + blockIdx.y * blockDim.y + threadIdx.y; i <= n - 2;
+         i += gridDim.y * blockDim.y) {
+        const long long row = (long long)i * ld;
+        const float4 a = ld4(u + row + x0);
+        const float4 c = ld4(g + row + x0);
+        float4 o;
+        o.x = __fadd_rn(a.x, c.x);
+        o.y = __fadd_rn(a.y, c.y);
+        o.z = __fadd_rn(a.z, c.z);
+        o.w = __fadd_rn(a.w, c.w);
+        store_interior(b + row, x0, n, o);
+    }
+}
+
+__global__ void k_copy_interior(const float *__restrict__ src,
+                                float *__restrict__ dst, int n, long long ld) {
+    const int x0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (x0 >= n) return;
+    for (int i = 1 + blockIdx.y * blockDim.y + threadIdx.y; i <= n - 2;
+         i += gridDim.y * blockDim.y) {
+        const long long row = (long long)i * ld;
+        store_interior(dst + row, x0, n, ld4(src + row + x0));
+    }
+}
+
+dim3 strip_grid(int n, int rows) {
+    const int nvec = (n + 3) / 4;
+    const int per_block = kWarps * rows;
+    return dim3((nvec + 31) / 32, (n - 2 + per_block - 1) / per_block);
+}
+
+dim3 elementwise_grid(int n) {
+    const int nvec = (n + 3) / 4;
+    const int gy = min((n - 2 + 7) / 8, 1024);
+    return dim3((nvec + 31) / 32, gy);
+}
+
+}  // namespace
+
+cudaError_t launch_rhs(const GridDesc &g, const float *u, const float *src,
+                       float *b, cudaStream_t stream) {
+    k_rhs<<<elementwise_grid(g.n), dim3(32, 8), 0, stream>>>(u, src, b, g.n,
+                                                              g.ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_interior(const GridDesc &g, const float *src,
+                                 float *dst, cudaStream_t stream) {
+    k_copy_interior<<<elementwise_grid(g.n), dim3(32, 8), 0, stream>>>(
+        src, dst, g.n, g.ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
+                              const float *b, float *out,
+                              cudaStream_t stream) {
+    k_sweep_sync<kSweepRows><<<strip_grid(g.n, kSweepRows), dim3(32, kWarps),
+                               0, stream>>>(u, b, out, g.n, g.ld, g.r, g.d);
+    return cudaGetLastError();
+}
+
+int residual_blocks(const GridDesc &g) {
+    const dim3 grid = strip_grid(g.n, kResidRows);
+    return (int)(grid.x * grid.y);
+}
+
+cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
+                            float *partials, ResidualOut *out,
+                            cudaGraphConditionalHandle, double,
+                            cudaStream_t stream) {
+    k_residual<kResidRows><<<strip_grid(g.n, kResidRows), dim3(32, kWarps), 0,
+                             stream>>>(u, b, g.n, g.ld, g.r, g.d,
+                                       reinterpret_cast<unsigned *>(partials),
+                                       out);
+    return cudaGetLastError();
+}
+
+}  // namespace tbj

@@ -1,0 +1,285 @@
+// TMA-staged tiled kernels: exact temporal blocking and block-asynchronous
+// sweeps ("Synchronous vs block-async Jacobi on one RTX 5050", section 02).
+//
+// A block owns one tile of TX x TY cells. Thread 0 issues three 2-D TMA box
+// loads onto one mbarrier: the box (tile plus halo) of the source field into
+// two shared buffers (the ping-pong pair) and the same box of b. The block
+// then runs D sweeps on chip, alternating buffers, and the last sweep writes
+// the tile's cells straight to the destination field in global memory.
+//
+//  * Exact temporal blocking (after Meng and Skadron): the halo is D cells
+//    deep; sweep s (0-based) updates the cells within D-1-s of the tile, so
+//    every value the next sweep reads is exact and after D sweeps the tile
+//    holds what D synchronous sweeps produce, bit for bit.
+//  * Block-asynchronous (after Anzt et al.): the halo is one cell deep and
+//    frozen at its value at launch; every sweep updates all tile cells.
+//
+// In both, cells on the Dirichlet ring and cells outside the grid (which the
+// TMA load fills with zeros) are never updated; no updated cell reads a cell
+// outside the grid. The box's left edge is kept on a 16-byte boundary (TMA
+// rule), so the halo loaded on the left is rounded up to a multiple of 4
+// columns; the extra columns are loaded and ignored.
+#include <cudaTypedefs.h>
+
+#include "jacobi_kernels.cuh"
+
+namespace tbj {
+namespace {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(count)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
+                                                      unsigned bytes) {
+    asm volatile(
+        "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase 0 of the barrier, giving up after ~1 s.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar) {
+    if (mbar_try_wait(bar, 0)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, 0)) {
+        if (global_ns() - t0 > 1000000000ull) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
+                                            uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
+        "complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_addr(bar))
+        : "memory");
+}
+
+__host__ __device__ constexpr size_t round128(size_t b) {
+    return (b + 127) / 128 * 128;
+}
+
+// Shared memory: [barrier | A | B | Bb], every part 128-byte aligned.
+__host__ __device__ inline size_t buffer_bytes(int box_x, int box_y) {
+    return round128((size_t)box_x * box_y * sizeof(float));
+}
+
+template <int D, bool EXACT>
+__global__ void __launch_bounds__(512)
+k_tiled(const __grid_constant__ CUtensorMap map_src,
+        const __grid_constant__ CUtensorMap map_b, float *__restrict__ out,
+        int n, long long ld, float r, float d, int tx, int ty, int hx, int hy,
+        int box_x, int box_y, int origin, ResidualOut *status) {
+    const int gx0 = origin + blockIdx.x * tx;  // tile's first cell (grid)
+    const int gy0 = origin + blockIdx.y * ty;
+    if (gx0 > n - 2 || gy0 > n - 2 || gx0 + tx <= 1 || gy0 + ty <= 1) return;
+    const int bxo = gx0 - hx;  // grid coordinates of box cell (0, 0)
+    const int byo = gy0 - hy;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base);
+    const size_t buf = buffer_bytes(box_x, box_y);
+    float *sA = reinterpret_cast<float *>(base + 128);
+    float *sB = reinterpret_cast<float *>(base + 128 + buf);
+    float *sBb = reinterpret_cast<float *>(base + 128 + 2 * buf);
+
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        const unsigned box_bytes = (unsigned)(box_x * box_y * sizeof(float));
+        mbar_arrive_expect_tx(bar, 3u * box_bytes);
+        tma_load_2d(sA, &map_src, bar, bxo, byo);
+        tma_load_2d(sB, &map_src, bar, bxo, byo);
+        tma_load_2d(sBb, &map_b, bar, bxo, byo);
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(bar);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) atomicOr(&status->err, (unsigned)ERR_TMA_TIMEOUT);
+        // Let any copy still in flight land before the block's shared
+        // memory is released (bounded as well).
+        mbar_wait_bounded(bar);
+        return;
+    }
+
+    // Box rows/columns whose grid cell is an interior cell.
+    const int vr0 = 1 - byo, vr1 = n - 1 - byo;  // [vr0, vr1)
+    const int vc0 = 1 - bxo, vc1 = n - 1 - bxo;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int nwarps = blockDim.x >> 5;
+
+#pragma unroll 1
+    for (int s = 0; s < D; ++s) {
+        const float *src = (s & 1) ? sB : sA;
+        float *dst = (s & 1) ? sA : sB;
+        const int e = EXACT ? (D - 1 - s) : 0;  // extension beyond the tile
+        const int r0 = max(hy - e, vr0), r1 = min(hy + ty + e, vr1);
+        const int c0 = max(hx - e, vc0), c1 = min(hx + tx + e, vc1);
+        const bool last = (s == D - 1);
+        for (int by = r0 + warp; by < r1; by += nwarps) {
+            const float *row = src + by * box_x;
+            const float *brow = sBb + by * box_x;
+            for (int bx = c0 + lane; bx < c1; bx += 32) {
+                const float v = jacobi_update(row[bx - 1], row[bx + 1],
+                                              row[bx - box_x], row[bx + box_x],
+                                              brow[bx], r, d);
+                if (last)
+                    out[(long long)(byo + by) * ld + (bxo + bx)] = v;
+                else
+                    dst[by * box_x + bx] = v;
+            }
+        }
+        if (!last) __syncthreads();
+    }
+}
+
+template <bool EXACT>
+cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
+                         const CUtensorMap *map_src, const CUtensorMap *map_b,
+                         float *out, ResidualOut *status,
+                         cudaStream_t stream) {
+    const dim3 grid((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x,
+                    (g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
+    const dim3 block(tc.threads);
+#define TBJ_LAUNCH(DD)                                                        \
+    case DD: {                                                                \
+        k_tiled<DD, EXACT><<<grid, block, tc.smem, stream>>>(                 \
+            *map_src, *map_b, out, g.n, g.ld, g.r, g.d, tc.tile_x, tc.tile_y, \
+            tc.halo_x, tc.halo_y, tc.box_x, tc.box_y, tc.origin, status);     \
+        return cudaGetLastError();                                            \
+    }
+    switch (tc.depth) {
+        TBJ_LAUNCH(1)
+        TBJ_LAUNCH(2)
+        TBJ_LAUNCH(4)
+        TBJ_LAUNCH(8)
+        TBJ_LAUNCH(16)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef TBJ_LAUNCH
+}
+
+template <bool EXACT>
+cudaError_t prepare_tiled(const TileConf &tc) {
+#define TBJ_PREP(DD)                                                          \
+    case DD:                                                                  \
+        return cudaFuncSetAttribute(k_tiled<DD, EXACT>,                       \
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                    (int)tc.smem);
+    switch (tc.depth) {
+        TBJ_PREP(1)
+        TBJ_PREP(2)
+        TBJ_PREP(4)
+        TBJ_PREP(8)
+        TBJ_PREP(16)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef TBJ_PREP
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+int finish_conf(TileConf *tc) {
+    if (tc->box_x > 256 || tc->box_y > 256 || tc->box_x % 4 != 0) return -5;
+    tc->smem = 128 + 128 + 3 * buffer_bytes(tc->box_x, tc->box_y);
+    if (tc->smem > kMaxSmem) return -5;
+    return 0;
+}
+
+}  // namespace
+
+int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
+    if (depth != 2 && depth != 4 && depth != 8 && depth != 16) return -1;
+    if (tile_x == 0) tile_x = 128;
+    if (tile_y == 0) tile_y = depth >= 16 ? 64 : 48;
+    if (tile_x < 4 || tile_x % 4 != 0 || tile_y < 1) return -1;
+    (void)n;
+    tc->depth = depth;
+    tc->tile_x = tile_x;
+    tc->tile_y = tile_y;
+    tc->halo_x = (depth + 3) / 4 * 4;
+    tc->halo_y = depth;
+    tc->box_x = tile_x + 2 * tc->halo_x;
+    tc->box_y = tile_y + 2 * depth;
+    tc->origin = 0;
+    tc->threads = 512;
+    return finish_conf(tc);
+}
+
+int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
+    if (depth != 1 && depth != 2 && depth != 4 && depth != 8 && depth != 16)
+        return -1;
+    if (tile_x == 0) tile_x = 32;
+    if (tile_y == 0) tile_y = 8;
+    if (tile_x < 4 || tile_x % 4 != 0 || tile_y < 1) return -1;
+    (void)n;
+    tc->depth = depth;
+    tc->tile_x = tile_x;
+    tc->tile_y = tile_y;
+    tc->halo_x = 1;  // box starts one column left of the tile (aligned:
+                     // the tile starts at 1 + k * tile_x)
+    tc->halo_y = 1;
+    tc->box_x = tile_x + 4;  // tile + 2 halo columns, rounded to 16 bytes
+    tc->box_y = tile_y + 2;
+    tc->origin = 1;
+    const int cells = tile_x * tile_y;
+    tc->threads = cells >= 512 ? 512 : (cells + 31) / 32 * 32;
+    return finish_conf(tc);
+}
+
+cudaError_t prepare_sweep_etb(const TileConf &tc) {
+    return prepare_tiled<true>(tc);
+}
+
+cudaError_t prepare_sweep_ba(const TileConf &tc) {
+    return prepare_tiled<false>(tc);
+}
+
+cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
+                             const CUtensorMap *map_src,
+                             const CUtensorMap *map_b, float *out,
+                             ResidualOut *status, cudaStream_t stream) {
+    return launch_tiled<true>(g, tc, map_src, map_b, out, status, stream);
+}
+
+cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
+                            const CUtensorMap *map_src,
+                            const CUtensorMap *map_b, float *out,
+                            ResidualOut *status, cudaStream_t stream) {
+    return launch_tiled<false>(g, tc, map_src, map_b, out, status, stream);
+}
+
+}  // namespace tbj

@@ -1,0 +1,226 @@
+"""Thin ctypes binding of the C ABI in include/jacobi.h.
+
+Argument marshalling only: every step of the solver runs in the CUDA kernels
+of libtbjacobi.so. PyTorch supplies device memory and the stream. There is no
+CPU fallback: if the library has not been built, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+SYNC, EXACT_TEMPORAL_BLOCKED, BLOCK_ASYNC = 0, 1, 2
+CONTROL_HOST, CONTROL_DEVICE = 0, 1
+OK, ERR_INVALID_ARG, ERR_CUDA, ERR_NOT_CONVERGED, ERR_NONFINITE, \
+    ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
+
+STRATEGIES = {"sync": SYNC, "etb": EXACT_TEMPORAL_BLOCKED,
+              "exact_temporal_blocked": EXACT_TEMPORAL_BLOCKED,
+              "ba": BLOCK_ASYNC, "block_async": BLOCK_ASYNC}
+CONTROLS = {"host": CONTROL_HOST, "device": CONTROL_DEVICE}
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("strategy", ctypes.c_int), ("depth", ctypes.c_int),
+                ("tile_x", ctypes.c_int), ("tile_y", ctypes.c_int),
+                ("check_every", ctypes.c_int), ("tol", ctypes.c_double),
+                ("max_sweeps", ctypes.c_longlong), ("control", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
+
+
+class JacobiError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libtbjacobi.so (it must have been built by __graft_entry__.build()
+    or temporal_blocked_jacobi_gb300._build.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing; build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp, ll, i, f = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
+        cfgp = ctypes.POINTER(Config)
+        sig = {
+            "jacobi_config_default": (i, [cfgp]),
+            "jacobi_create": (i, [ctypes.POINTER(vp), i, ll, f, cfgp, vp, vp, vp, vp]),
+            "jacobi_rhs": (i, [vp, vp]),
+            "jacobi_solve_step": (ll, [vp]),
+            "jacobi_sweeps": (ll, [vp, ll]),
+            "jacobi_residual": (i, [vp, ctypes.POINTER(f), ctypes.POINTER(f)]),
+            "jacobi_set_strategy": (i, [vp, cfgp]),
+            "jacobi_run": (ll, [vp, vp, i, ctypes.POINTER(ll)]),
+            "jacobi_launch_count": (ll, [vp]),
+            "jacobi_destroy": (None, [vp]),
+            "jacobi_last_error": (ctypes.c_char_p, [vp]),
+            "jacobi_status_string": (ctypes.c_char_p, [i]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().jacobi_status_string(int(status)).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
+                tol=1e-5, max_sweeps=1 << 22, control="host") -> Config:
+    c = Config()
+    load().jacobi_config_default(ctypes.byref(c))
+    c.strategy = STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
+    c.depth = int(depth)
+    c.tile_x, c.tile_y = int(tile[0]), int(tile[1])
+    c.check_every = int(check_every)
+    c.tol = float(tol)
+    c.max_sweeps = int(max_sweeps)
+    c.control = CONTROLS[control] if isinstance(control, str) else int(control)
+    return c
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_field(t, shape=None):
+    import torch
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32
+            and t.dim() == 2 and t.is_contiguous()):
+        raise ValueError("fields must be contiguous 2-D float32 CUDA tensors")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"field shape {tuple(t.shape)} != {tuple(shape)}")
+
+
+def allocate(n: int, ld: int | None = None, device="cuda"):
+    """Three zeroed (n, ld) float32 device fields for u, u_alt and b."""
+    import torch
+    ld = (n + 3) // 4 * 4 if ld is None else ld
+    return tuple(torch.zeros((n, ld), dtype=torch.float32, device=device)
+                 for _ in range(3))
+
+
+class Solver:
+    """One solver handle over caller-owned fields u, u_alt, b of shape (N, ld).
+
+    u holds uⁿ with its Dirichlet ring on entry; each solved step leaves the
+    new iterate in u. All work is enqueued on `stream` (default: the current
+    torch stream)."""
+
+    def __init__(self, u, u_alt, b, r, *, strategy="sync", depth=1,
+                 tile=(0, 0), check_every=8, tol=1e-5, max_sweeps=1 << 22,
+                 control="host", stream=None):
+        import torch
+        lib = load()
+        for t in (u, u_alt, b):
+            _check_field(t, u.shape)
+        self.n, self.ld = int(u.shape[0]), int(u.shape[1])
+        self.u, self.u_alt, self.b = u, u_alt, b
+        self.stream = torch.cuda.current_stream(u.device) if stream is None else stream
+        self._h = ctypes.c_void_p()
+        cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps, control)
+        with torch.cuda.device(u.device):
+            rc = lib.jacobi_create(ctypes.byref(self._h), self.n, self.ld,
+                                   float(r), ctypes.byref(cfg), _ptr(u),
+                                   _ptr(u_alt), _ptr(b),
+                                   ctypes.c_void_p(self.stream.cuda_stream))
+        if rc != OK:
+            raise JacobiError(rc, lib.jacobi_last_error(None).decode())
+        self.r = float(r)
+        self.config = cfg
+
+    # -- helpers -----------------------------------------------------------
+    def _raise(self, status):
+        raise JacobiError(int(status), load().jacobi_last_error(self._h).decode())
+
+    def _ok(self, rc):
+        if rc < 0:
+            self._raise(rc)
+        return rc
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise RuntimeError("solver is closed")
+        return self._h
+
+    # -- C ABI ---------------------------------------------------------------
+    def rhs(self, g):
+        _check_field(g, self.u.shape)
+        self._ok(load().jacobi_rhs(self.handle, _ptr(g)))
+
+    def solve_step(self, raise_on_error=True) -> int:
+        k = load().jacobi_solve_step(self.handle)
+        return self._ok(k) if raise_on_error else k
+
+    def sweeps(self, launches: int) -> int:
+        return self._ok(load().jacobi_sweeps(self.handle, int(launches)))
+
+    def residual(self):
+        rm, bm = ctypes.c_float(), ctypes.c_float()
+        self._ok(load().jacobi_residual(self.handle, ctypes.byref(rm), ctypes.byref(bm)))
+        return rm.value, bm.value
+
+    def set_strategy(self, strategy="sync", depth=1, tile=(0, 0),
+                     check_every=8, tol=1e-5, max_sweeps=1 << 22, control="host"):
+        cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps, control)
+        self._ok(load().jacobi_set_strategy(self.handle, ctypes.byref(cfg)))
+        self.config = cfg
+
+    def run(self, g, steps=10):
+        """`steps` backward-Euler steps; returns the list of sweeps per step."""
+        _check_field(g, self.u.shape)
+        counts = (ctypes.c_longlong * max(steps, 1))()
+        total = load().jacobi_run(self.handle, _ptr(g), int(steps), counts)
+        if total < 0:
+            self._raise(total)
+        return [int(counts[s]) for s in range(steps)]
+
+    @property
+    def launch_count(self) -> int:
+        return int(load().jacobi_launch_count(self.handle))
+
+    @property
+    def last_error(self) -> str:
+        return load().jacobi_last_error(self.handle).decode()
+
+    def close(self):
+        if self._h:
+            load().jacobi_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

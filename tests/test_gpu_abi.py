@@ -1,0 +1,120 @@
+"""Status codes of the C ABI: bad arguments are rejected, the sweep cap and
+non-finite residuals are reported, and the handle stays usable after."""
+import numpy as np
+import pytest
+
+from temporal_blocked_jacobi_gb300 import problem as P
+from tests.gpu_helpers import to_dev, workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _jacobi():
+    from temporal_blocked_jacobi_gb300 import jacobi
+    return jacobi
+
+
+def test_invalid_arguments_rejected():
+    import torch
+    jacobi = _jacobi()
+    u, u_alt, b = jacobi.allocate(32, 32)
+    with pytest.raises(jacobi.JacobiError) as e:  # ld not a multiple of 4
+        x = torch.zeros((32, 34), device="cuda")
+        jacobi.Solver(x, x.clone(), x.clone(), 1.0)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    with pytest.raises(jacobi.JacobiError) as e:  # n < 3
+        x = torch.zeros((2, 4), device="cuda")
+        jacobi.Solver(x, x.clone(), x.clone(), 1.0)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    with pytest.raises(jacobi.JacobiError) as e:  # aliased buffers
+        jacobi.Solver(u, u, b, 1.0)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    with pytest.raises(jacobi.JacobiError) as e:  # negative r
+        jacobi.Solver(u, u_alt, b, -1.0)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    with pytest.raises(jacobi.JacobiError) as e:  # bad depth
+        jacobi.Solver(u, u_alt, b, 1.0, strategy="etb", depth=3)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    with pytest.raises(jacobi.JacobiError) as e:  # box wider than TMA allows
+        jacobi.Solver(u, u_alt, b, 1.0, strategy="etb", depth=16, tile=(248, 8))
+    assert e.value.status == jacobi.ERR_UNSUPPORTED
+    with pytest.raises(jacobi.JacobiError) as e:  # tile_x not a multiple of 4
+        jacobi.Solver(u, u_alt, b, 1.0, strategy="ba", depth=4, tile=(30, 8))
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    # misaligned (4-byte offset) view
+    big = torch.zeros(32 * 32 + 4, device="cuda")
+    mis = big[1:1 + 32 * 32].view(32, 32)
+    with pytest.raises(jacobi.JacobiError) as e:
+        jacobi.Solver(mis, u_alt, b, 1.0)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+
+
+def test_host_buffers_rejected():
+    import ctypes
+    jacobi = _jacobi()
+    lib = jacobi.load()
+    hosts = [np.zeros((16, 16), dtype=np.float32) for _ in range(3)]
+    h = ctypes.c_void_p()
+    p = [a.ctypes.data_as(ctypes.c_void_p) for a in hosts]
+    rc = lib.jacobi_create(ctypes.byref(h), 16, 16, 1.0, None, p[0], p[1],
+                           p[2], None)
+    assert rc == jacobi.ERR_INVALID_ARG
+    assert not h.value
+
+
+def test_sweep_cap_not_converged_then_recovers():
+    import torch
+    jacobi = _jacobi()
+    n, r = 128, 100.0
+    u0, g = workload(n, "point")
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    with jacobi.Solver(u, u_alt, b, r, max_sweeps=24) as s:
+        s.rhs(to_dev(g))
+        k = s.solve_step(raise_on_error=False)
+        assert k == jacobi.ERR_NOT_CONVERGED
+        assert "not converged" in s.last_error
+        s.set_strategy("sync", 1, max_sweeps=1 << 22)
+        assert s.solve_step() > 0
+    torch.cuda.synchronize()
+
+
+def test_nan_source_reports_nonfinite():
+    jacobi = _jacobi()
+    n = 64
+    u0, g = workload(n, "gauss")
+    g[10, 12] = np.nan
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    for kw in ({}, {"strategy": "etb", "depth": 4}, {"strategy": "ba", "depth": 2}):
+        u.copy_(to_dev(u0))
+        with jacobi.Solver(u, u_alt, b, 1.0, **kw) as s:
+            s.rhs(to_dev(g))
+            assert s.solve_step(raise_on_error=False) == jacobi.ERR_NONFINITE
+
+
+def test_zero_problem_converges_at_first_check():
+    jacobi = _jacobi()
+    n = 50
+    u0 = P.initial_field(n, top=0.0)
+    g = P.source_term(n, kind="zero")
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    with jacobi.Solver(u, u_alt, b, 10.0, strategy="etb", depth=8) as s:
+        s.rhs(to_dev(g))
+        assert s.solve_step() == 8
+        assert s.residual() == (0.0, 0.0)
+
+
+def test_launch_count_grows():
+    jacobi = _jacobi()
+    n = 40
+    u0, g = workload(n, "point")
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    with jacobi.Solver(u, u_alt, b, 1.0) as s:
+        c0 = s.launch_count
+        s.rhs(to_dev(g))
+        k = s.solve_step()
+        # rhs + k sweeps + one residual per check interval of 8
+        assert s.launch_count - c0 == 1 + k + k // 8
