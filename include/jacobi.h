@@ -143,6 +143,39 @@ long long jacobi_sweeps(jacobi_handle_t *h, long long launches);
 int jacobi_residual(jacobi_handle_t *h, float *rmax, float *bmax);
 
 /*
+ * Residual norms without any allocation. The page has no counterpart for
+ * this call; it exists for callers that cannot call cudaMalloc when they need
+ * the norms: code running while a stream is being captured into a CUDA
+ * graph, loops that must not pay for the device-wide synchronisation that
+ * cudaMalloc/cudaFree imply, and applications whose device memory is handed
+ * out only by their own allocator.
+ *
+ * It computes what jacobi_residual computes, for any u and b in the grid
+ * layout, without a handle: norms[0] = rmax = max over the interior of
+ * d |J(u) - u|, norms[1] = bmax = max |b_ij + r (sum of the cell's
+ * Dirichlet-ring neighbours)|, d = 1 + 4r. u, b: device, N*ld floats,
+ * 16-byte aligned. norms: device, 2 floats, written asynchronously on
+ * cuda_stream (a stream of the current device; NULL = legacy default).
+ *
+ * Scratch: a fixed array in the library's device memory, reserved on every
+ * GPU that loads the library until the process exits (about 256 KiB). All
+ * calls share it, so calls that could overlap on the GPU (other streams,
+ * other host threads) race and must be serialised by the caller. The first
+ * call on each device looks up the array's device address; make that first
+ * call before any stream capture. It calls no allocating routine.
+ *
+ * Returns JACOBI_OK, JACOBI_ERR_INVALID_ARG (sizes, pitch, r, NULL or
+ * misaligned pointers), JACOBI_ERR_UNSUPPORTED when N exceeds
+ * JACOBI_RESIDUAL_NOALLOC_MAX_N (the scratch holds partial maxima for at most
+ * JACOBI_RESIDUAL_NOALLOC_MAX_BLOCKS reduction blocks; nothing is launched),
+ * or JACOBI_ERR_CUDA.
+ */
+#define JACOBI_RESIDUAL_NOALLOC_MAX_BLOCKS 32768
+#define JACOBI_RESIDUAL_NOALLOC_MAX_N 23168
+int jacobi_residual_noalloc(int n, long long ld, float r, const float *u,
+                            const float *b, float *norms, void *cuda_stream);
+
+/*
  * Change strategy, depth, tile, tolerance or control between steps
  * (section 02: D is a launch parameter, so switching it costs nothing).
  * Rebuilds the handle's graphs. u must hold the current iterate.

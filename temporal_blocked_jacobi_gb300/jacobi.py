@@ -73,6 +73,7 @@ def load():
             "jacobi_destroy": (None, [vp]),
             "jacobi_last_error": (ctypes.c_char_p, [vp]),
             "jacobi_status_string": (ctypes.c_char_p, [i]),
+            "jacobi_residual_noalloc": (i, [i, ll, f, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -87,6 +88,25 @@ def status_string(status: int) -> str:
         return load().jacobi_status_string(int(status)).decode()
     except Exception:
         return f"status {status}"
+
+
+def residual_noalloc(u, b, r, norms, stream=None) -> int:
+    """jacobi_residual_noalloc: residual norms of any (u, b) pair into the
+    device tensor `norms` (2 floats: rmax, bmax) without allocating anything;
+    asynchronous on `stream` (default: the current torch stream). Returns the
+    status code (0 on success) instead of raising, so it can be used where
+    exceptions are unwelcome."""
+    import torch
+    _check_field(u)
+    _check_field(b, u.shape)
+    if not (isinstance(norms, torch.Tensor) and norms.is_cuda
+            and norms.dtype == torch.float32 and norms.numel() >= 2
+            and norms.is_contiguous()):
+        raise ValueError("norms must be a contiguous float32 CUDA tensor of 2 elements")
+    stream = torch.cuda.current_stream(u.device) if stream is None else stream
+    return int(load().jacobi_residual_noalloc(
+        int(u.shape[0]), int(u.shape[1]), float(r), _ptr(u), _ptr(b),
+        _ptr(norms), ctypes.c_void_p(stream.cuda_stream)))
 
 
 def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
