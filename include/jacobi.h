@@ -69,6 +69,18 @@ typedef enum {
     JACOBI_CONTROL_DEVICE = 1
 } jacobi_control_t;
 
+/* How the kernels divide by d = 1 + 4r. Both give the correctly rounded
+ * float32 quotient for every finite numerator, so results are identical. */
+typedef enum {
+    /* Use a fixed-divisor division (one multiply and two fused multiply-adds
+     * with the precomputed RN(1/d)) if an exhaustive check against IEEE
+     * division over all finite float32 numerators passes for this d (run
+     * once per distinct d, about a millisecond); otherwise IEEE division. */
+    JACOBI_DIVISION_AUTO = 0,
+    /* Always the IEEE division instruction sequence. */
+    JACOBI_DIVISION_IEEE = 1
+} jacobi_division_t;
+
 typedef struct {
     int strategy;         /* jacobi_strategy_t */
     int depth;            /* D: SYNC 1; EXACT_TEMPORAL_BLOCKED 2,4,8,16; BLOCK_ASYNC 1,2,4,8,16 */
@@ -79,7 +91,8 @@ typedef struct {
     double tol;           /* stop when rmax < tol * bmax (or rmax == 0); default 1e-5 */
     long long max_sweeps; /* give up (JACOBI_ERR_NOT_CONVERGED) at this many sweeps; default 1<<22 */
     int control;          /* jacobi_control_t; default JACOBI_CONTROL_HOST */
-    int reserved[3];      /* must be 0 */
+    int division;         /* jacobi_division_t; default JACOBI_DIVISION_AUTO */
+    int reserved[2];      /* must be 0 */
 } jacobi_config_t;
 
 typedef struct jacobi_handle jacobi_handle_t;
@@ -190,6 +203,10 @@ int jacobi_set_strategy(jacobi_handle_t *h, const jacobi_config_t *cfg);
  */
 long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
                      long long *sweeps_per_step);
+
+/* Division the handle's kernels use: 1 = verified fixed-divisor division,
+ * 0 = IEEE division, < 0 = error (NULL handle). */
+int jacobi_division_mode(const jacobi_handle_t *h);
 
 /* Number of kernels this handle has launched so far (graph nodes included). */
 long long jacobi_launch_count(const jacobi_handle_t *h);

@@ -8,6 +8,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
 
 #include "../../include/jacobi.h"
@@ -122,9 +124,11 @@ long long gcd_ll(long long a, long long b) {
 }
 
 int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
-    for (int k = 0; k < 3; ++k)
+    for (int k = 0; k < 2; ++k)
         if (c.reserved[k])
             return fail(h, JACOBI_ERR_INVALID_ARG, "reserved fields must be 0");
+    if (c.division != JACOBI_DIVISION_AUTO && c.division != JACOBI_DIVISION_IEEE)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "unknown division %d", c.division);
     if (c.check_every < 1)
         return fail(h, JACOBI_ERR_INVALID_ARG, "check_every must be >= 1");
     if (!(c.tol >= 0.0) || !std::isfinite(c.tol))
@@ -215,10 +219,52 @@ int record_batch(jacobi_handle_t *h, int start, cudaGraphExec_t *exec) {
     return JACOBI_OK;
 }
 
+// Is the fixed-divisor division bit-identical to IEEE division for every
+// finite numerator with this d? Checked exhaustively on the device once per
+// distinct d per process.
+std::mutex g_fastdiv_mutex;
+std::map<unsigned, bool> g_fastdiv_ok;
+
+int fast_division_ok(jacobi_handle_t *h, bool *ok) {
+    unsigned key;
+    std::memcpy(&key, &h->g.d, sizeof key);
+    {
+        std::lock_guard<std::mutex> lock(g_fastdiv_mutex);
+        auto it = g_fastdiv_ok.find(key);
+        if (it != g_fastdiv_ok.end()) {
+            *ok = it->second;
+            return JACOBI_OK;
+        }
+    }
+    unsigned long long *count = nullptr, host = ~0ull;
+    cudaError_t e = cudaMalloc(&count, sizeof *count);
+    if (e == cudaSuccess) e = cudaMemsetAsync(count, 0, sizeof *count, h->stream);
+    if (e == cudaSuccess) e = fastdiv_verify_launch(h->g.d, h->g.y, count, h->stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&host, count, sizeof host, cudaMemcpyDeviceToHost,
+                            h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (count) cudaFree(count);
+    if (e != cudaSuccess)
+        return fail(h, JACOBI_ERR_CUDA, "checking the fixed-divisor division: %s",
+                    cudaGetErrorString(e));
+    *ok = (host == 0);
+    std::lock_guard<std::mutex> lock(g_fastdiv_mutex);
+    g_fastdiv_ok[key] = *ok;
+    return JACOBI_OK;
+}
+
 // Apply a (validated) configuration: tiles, tensor maps, graphs.
 int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     destroy_graphs(h);
     h->cfg = c;
+    h->g.fast = false;
+    if (c.division == JACOBI_DIVISION_AUTO) {
+        bool ok = false;
+        int rc = fast_division_ok(h, &ok);
+        if (rc) return rc;
+        h->g.fast = ok;
+    }
     int rc = 0;
     if (c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED)
         rc = etb_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc);
@@ -286,6 +332,7 @@ int jacobi_config_default(jacobi_config_t *cfg) {
     cfg->tol = 1e-5;
     cfg->max_sweeps = 1ll << 22;
     cfg->control = JACOBI_CONTROL_HOST;
+    cfg->division = JACOBI_DIVISION_AUTO;
     return JACOBI_OK;
 }
 
@@ -328,6 +375,8 @@ int jacobi_create(jacobi_handle_t **out, int n, long long ld, float r,
         // d = fl(1 + fl(4 r)) in float32 (host code, -ffp-contract=off).
         volatile float four_r = 4.0f * r;
         h->g.d = 1.0f + four_r;
+        h->g.y = reciprocal_rn(h->g.d);
+        h->g.fast = false;
     }
     h->u = u;
     h->u_alt = u_alt;
@@ -459,6 +508,11 @@ long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
         total += k;
     }
     return total;
+}
+
+int jacobi_division_mode(const jacobi_handle_t *h) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    return h->g.fast ? 1 : 0;
 }
 
 long long jacobi_launch_count(const jacobi_handle_t *h) {

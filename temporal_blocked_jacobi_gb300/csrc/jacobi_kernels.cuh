@@ -9,22 +9,61 @@
 namespace tbj {
 
 // ---------------------------------------------------------------------------
+// Correctly rounded division by the fixed diagonal d.
+//
+// All kernels divide by the same d = 1 + 4r. With y = RN(1/d) the quotient
+// is refined once from q0 = RN(x*y) using the exact remainder (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990; the remainder of a faithful
+// quotient is exact in one fused multiply-add):
+//     q0  = RN(x * y)
+//     rho = RN(q0 * d - x)        (exact)
+//     q   = RN(q0 - rho * y)
+// The remainder is formed with its sign flipped so that x = -0 yields -0.
+// Whether this equals the IEEE quotient for EVERY finite x depends on d, so
+// each handle checks it exhaustively against __fdiv_rn for its own d (all
+// finite float32 numerators) before using it (fastdiv_verify); otherwise
+// the kernels use __fdiv_rn. A non-finite numerator gives a non-finite
+// result either way (NaN where IEEE gives +-Inf).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float div_fixed(float x, float d, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float rho = __fmaf_rn(q0, d, -x);
+    return __fmaf_rn(-rho, y, q0);
+}
+
+template <bool FAST>
+__device__ __forceinline__ float div_d(float x, float d, float y) {
+    if (FAST) return div_fixed(x, d, y);
+    return __fdiv_rn(x, d);
+}
+
+// ---------------------------------------------------------------------------
 // The update of "Synchronous vs block-async Jacobi on one RTX 5050",
 // sections 01-02: J(u)_ij = (b_ij + r * ((uW + uE) + (uN + uS))) / d,
 // d = 1 + 4r. Round-to-nearest intrinsics fix the order and keep the
 // compiler from fusing the multiply into the add; the division is the
-// correctly rounded IEEE quotient.
+// correctly rounded quotient.
 // ---------------------------------------------------------------------------
+template <bool FAST = false>
 __device__ __forceinline__ float jacobi_update(float uw, float ue, float un,
                                                float us, float b, float r,
-                                               float d) {
+                                               float d, float y = 0.f) {
     float horiz = __fadd_rn(uw, ue);
     float vert = __fadd_rn(un, us);
     float s = __fadd_rn(horiz, vert);
     float rs = __fmul_rn(r, s);
     float num = __fadd_rn(b, rs);
-    return __fdiv_rn(num, d);
+    return div_d<FAST>(num, d, y);
 }
+
+// Exhaustive check of div_fixed against __fdiv_rn for one d: counts the
+// finite float32 numerators whose quotients differ in any bit. `count` is a
+// device word (set to 0 by the caller). Launch fastdiv_verify_launch.
+cudaError_t fastdiv_verify_launch(float d, float y, unsigned long long *count,
+                                  cudaStream_t stream);
+// RN(1/d) in float32, computed exactly on the host.
+float reciprocal_rn(float d);
 
 // Error bits written by kernels into the handle's status word.
 enum : unsigned {
@@ -37,6 +76,8 @@ struct GridDesc {
     long long ld;  // row pitch in floats
     float r;       // coupling alpha dt / h^2
     float d;       // fl(1 + fl(4 r))
+    float y;       // RN(1/d)
+    bool fast;     // div_fixed verified equal to IEEE division for this d
 };
 
 // Result block of a residual reduction (device memory, one per handle).
@@ -68,13 +109,14 @@ struct TileConf {
     int depth;    // D
     int tile_x;   // TX, multiple of 4
     int tile_y;   // TY
-    int halo_x;   // columns loaded beyond the tile on each side (multiple of 4)
-    int halo_y;   // rows loaded beyond the tile on each side
+    int halo_x;   // box columns left of the tile (a multiple of 4 for ETB)
+    int halo_y;   // box rows above the tile
     int box_x;    // TX + 2 * halo_x  (<= 256)
     int box_y;    // TY + 2 * halo_y  (<= 256)
     int origin;   // grid coordinate of the first tile's first cell (0 or 1)
     int threads;  // block size
     size_t smem;  // dynamic shared memory bytes
+    int variant;  // compiled shape (exact temporal blocking)
 };
 
 // Exact temporal blocking (section 02 "Exact temporal blocking", after Meng

@@ -15,9 +15,18 @@ namespace tbj {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int kWarps = 4;       // warps per block, stacked vertically
-constexpr int kSweepRows = 16;  // rows per warp in a sweep
-constexpr int kResidRows = 32;  // rows per warp in the residual
+constexpr int kWarps = 4;  // warps per block, stacked vertically
+
+// Rows per warp: the largest of 32, 16, 8, 4 that still gives at least
+// ~54 resident warps' worth of strips per SM on 152 SMs, so small grids
+// keep enough loads in flight.
+int rows_per_warp(int n) {
+    const long long strips = ((n + 3) / 4 + 31) / 32;
+    for (int rows : {32, 16, 8}) {
+        if (strips * ((n - 2 + rows - 1) / rows) >= 8192) return rows;
+    }
+    return 4;
+}
 
 __device__ __forceinline__ float4 ld4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
@@ -69,10 +78,11 @@ __device__ __forceinline__ RowIn load_row(const float *__restrict__ u,
 // Synchronous sweep u -> out (section 02 "Synchronous"): every interior cell
 // gets J(u); the ring of out is never written.
 // ---------------------------------------------------------------------------
-template <int ROWS>
+template <int ROWS, bool FAST>
 __global__ void __launch_bounds__(32 * kWarps)
 k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
-             float *__restrict__ out, int n, long long ld, float r, float d) {
+             float *__restrict__ out, int n, long long ld, float r, float d,
+             float y) {
     const int lane = threadIdx.x;
     const int vx = blockIdx.x * 32 + lane;
     const int x0 = vx * 4;
@@ -95,10 +105,10 @@ k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
         if (lane == 0) west = cur.edge;
         if (lane == 31) east = cur.edge;
         float4 o;
-        o.x = jacobi_update(west, mid.y, top.x, cur.bot.x, cur.bb.x, r, d);
-        o.y = jacobi_update(mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, r, d);
-        o.z = jacobi_update(mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, r, d);
-        o.w = jacobi_update(mid.z, east, top.w, cur.bot.w, cur.bb.w, r, d);
+        o.x = jacobi_update<FAST>(west, mid.y, top.x, cur.bot.x, cur.bb.x, r, d, y);
+        o.y = jacobi_update<FAST>(mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, r, d, y);
+        o.z = jacobi_update<FAST>(mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, r, d, y);
+        o.w = jacobi_update<FAST>(mid.z, east, top.w, cur.bot.w, cur.bb.w, r, d, y);
         if (active) store_interior(out + (long long)i * ld, x0, n, o);
         top = mid;
         mid = cur.bot;
@@ -121,13 +131,14 @@ __device__ __forceinline__ unsigned fbits(float x) {
     return __float_as_uint(fabsf(x));
 }
 
+template <bool FAST>
 __device__ __forceinline__ void cell_norms(float c, float west, float east,
                                            float north, float south, float bb,
                                            int i, int x, int n, float r,
-                                           float d, unsigned &rm,
+                                           float d, float y, unsigned &rm,
                                            unsigned &bm) {
     if (x < 1 || x > n - 2) return;
-    const float ju = jacobi_update(west, east, north, south, bb, r, d);
+    const float ju = jacobi_update<FAST>(west, east, north, south, bb, r, d, y);
     const float e = __fmul_rn(d, fabsf(__fsub_rn(ju, c)));
     const float qw = (x - 1 == 0) ? west : 0.f;
     const float qe = (x + 1 == n - 1) ? east : 0.f;
@@ -145,11 +156,11 @@ __device__ __forceinline__ unsigned warp_max(unsigned v) {
     return v;
 }
 
-template <int ROWS>
+template <int ROWS, bool FAST>
 __global__ void __launch_bounds__(32 * kWarps)
 k_residual(const float *__restrict__ u, const float *__restrict__ b, int n,
-           long long ld, float r, float d, unsigned *__restrict__ partials,
-           ResidualOut *__restrict__ out) {
+           long long ld, float r, float d, float y,
+           unsigned *__restrict__ partials, ResidualOut *__restrict__ out) {
     const int lane = threadIdx.x;
     const int vx = blockIdx.x * 32 + lane;
     const int x0 = vx * 4;
@@ -172,10 +183,10 @@ k_residual(const float *__restrict__ u, const float *__restrict__ b, int n,
             if (lane == 0) west = cur.edge;
             if (lane == 31) east = cur.edge;
             if (active) {
-                cell_norms(mid.x, west, mid.y, top.x, cur.bot.x, cur.bb.x, i, x0 + 0, n, r, d, rm, bm);
-                cell_norms(mid.y, mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, i, x0 + 1, n, r, d, rm, bm);
-                cell_norms(mid.z, mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, i, x0 + 2, n, r, d, rm, bm);
-                cell_norms(mid.w, mid.z, east, top.w, cur.bot.w, cur.bb.w, i, x0 + 3, n, r, d, rm, bm);
+                cell_norms<FAST>(mid.x, west, mid.y, top.x, cur.bot.x, cur.bb.x, i, x0 + 0, n, r, d, y, rm, bm);
+                cell_norms<FAST>(mid.y, mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, i, x0 + 1, n, r, d, y, rm, bm);
+                cell_norms<FAST>(mid.z, mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, i, x0 + 2, n, r, d, y, rm, bm);
+                cell_norms<FAST>(mid.w, mid.z, east, top.w, cur.bot.w, cur.bb.w, i, x0 + 3, n, r, d, y, rm, bm);
             }
             top = mid;
             mid = cur.bot;
@@ -300,13 +311,31 @@ cudaError_t launch_copy_interior(const GridDesc &g, const float *src,
 cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
                               const float *b, float *out,
                               cudaStream_t stream) {
-    k_sweep_sync<kSweepRows><<<strip_grid(g.n, kSweepRows), dim3(32, kWarps),
-                               0, stream>>>(u, b, out, g.n, g.ld, g.r, g.d);
+    const int rows = rows_per_warp(g.n);
+    const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
+#define TBJ_SWEEP(R)                                                           \
+    case R:                                                                    \
+        if (g.fast)                                                            \
+            k_sweep_sync<R, true><<<grid, block, 0, stream>>>(u, b, out, g.n,  \
+                                                              g.ld, g.r, g.d,  \
+                                                              g.y);            \
+        else                                                                   \
+            k_sweep_sync<R, false><<<grid, block, 0, stream>>>(u, b, out, g.n, \
+                                                               g.ld, g.r, g.d, \
+                                                               g.y);           \
+        break;
+    switch (rows) {
+        TBJ_SWEEP(4)
+        TBJ_SWEEP(8)
+        TBJ_SWEEP(16)
+        TBJ_SWEEP(32)
+    }
+#undef TBJ_SWEEP
     return cudaGetLastError();
 }
 
 int residual_blocks(const GridDesc &g) {
-    const dim3 grid = strip_grid(g.n, kResidRows);
+    const dim3 grid = strip_grid(g.n, rows_per_warp(g.n));
     return (int)(grid.x * grid.y);
 }
 
@@ -314,10 +343,25 @@ cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
                             float *partials, ResidualOut *out,
                             cudaGraphConditionalHandle, double,
                             cudaStream_t stream) {
-    k_residual<kResidRows><<<strip_grid(g.n, kResidRows), dim3(32, kWarps), 0,
-                             stream>>>(u, b, g.n, g.ld, g.r, g.d,
-                                       reinterpret_cast<unsigned *>(partials),
-                                       out);
+    const int rows = rows_per_warp(g.n);
+    const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
+    unsigned *part = reinterpret_cast<unsigned *>(partials);
+#define TBJ_RESID(R)                                                          \
+    case R:                                                                   \
+        if (g.fast)                                                           \
+            k_residual<R, true><<<grid, block, 0, stream>>>(                  \
+                u, b, g.n, g.ld, g.r, g.d, g.y, part, out);                   \
+        else                                                                  \
+            k_residual<R, false><<<grid, block, 0, stream>>>(                 \
+                u, b, g.n, g.ld, g.r, g.d, g.y, part, out);                   \
+        break;
+    switch (rows) {
+        TBJ_RESID(4)
+        TBJ_RESID(8)
+        TBJ_RESID(16)
+        TBJ_RESID(32)
+    }
+#undef TBJ_RESID
     return cudaGetLastError();
 }
 

@@ -1,24 +1,19 @@
-// TMA-staged tiled kernels: exact temporal blocking and block-asynchronous
-// sweeps ("Synchronous vs block-async Jacobi on one RTX 5050", section 02).
+// Block-asynchronous sweeps ("Synchronous vs block-async Jacobi on one
+// RTX 5050", section 02, after Anzt et al.), TMA-staged.
 //
 // A block owns one tile of TX x TY cells. Thread 0 issues three 2-D TMA box
-// loads onto one mbarrier: the box (tile plus halo) of the source field into
-// two shared buffers (the ping-pong pair) and the same box of b. The block
-// then runs D sweeps on chip, alternating buffers, and the last sweep writes
-// the tile's cells straight to the destination field in global memory.
+// loads onto one mbarrier: the box (tile plus a one-cell halo) of the source
+// field into two shared buffers (the ping-pong pair) and the same box of b.
+// The halo is frozen at its value at launch; every one of the D sweeps
+// updates all tile cells, alternating buffers, and the last sweep writes the
+// tile's cells straight to the destination field in global memory.
 //
-//  * Exact temporal blocking (after Meng and Skadron): the halo is D cells
-//    deep; sweep s (0-based) updates the cells within D-1-s of the tile, so
-//    every value the next sweep reads is exact and after D sweeps the tile
-//    holds what D synchronous sweeps produce, bit for bit.
-//  * Block-asynchronous (after Anzt et al.): the halo is one cell deep and
-//    frozen at its value at launch; every sweep updates all tile cells.
-//
-// In both, cells on the Dirichlet ring and cells outside the grid (which the
-// TMA load fills with zeros) are never updated; no updated cell reads a cell
-// outside the grid. The box's left edge is kept on a 16-byte boundary (TMA
-// rule), so the halo loaded on the left is rounded up to a multiple of 4
-// columns; the extra columns are loaded and ignored.
+// Cells on the Dirichlet ring and cells outside the grid (which the TMA load
+// fills with zeros) are never updated; no updated cell reads a cell outside
+// the grid. The box's left edge is kept on a 16-byte boundary (TMA rule):
+// tiles start at column 1 + k*TX with TX a multiple of 4, so the box starts
+// at k*TX and is TX + 4 columns wide; the extra columns are loaded and
+// ignored.
 #include <cudaTypedefs.h>
 
 #include "jacobi_kernels.cuh"
@@ -93,12 +88,13 @@ __host__ __device__ inline size_t buffer_bytes(int box_x, int box_y) {
     return round128((size_t)box_x * box_y * sizeof(float));
 }
 
-template <int D, bool EXACT>
+template <int D, bool FAST>
 __global__ void __launch_bounds__(512)
-k_tiled(const __grid_constant__ CUtensorMap map_src,
-        const __grid_constant__ CUtensorMap map_b, float *__restrict__ out,
-        int n, long long ld, float r, float d, int tx, int ty, int hx, int hy,
-        int box_x, int box_y, int origin, ResidualOut *status) {
+k_block_async(const __grid_constant__ CUtensorMap map_src,
+              const __grid_constant__ CUtensorMap map_b,
+              float *__restrict__ out, int n, long long ld, float r, float d,
+              float y, int tx, int ty, int hx, int hy, int box_x, int box_y,
+              int origin, ResidualOut *status) {
     const int gx0 = origin + blockIdx.x * tx;  // tile's first cell (grid)
     const int gy0 = origin + blockIdx.y * ty;
     if (gx0 > n - 2 || gy0 > n - 2 || gx0 + tx <= 1 || gy0 + ty <= 1) return;
@@ -143,17 +139,16 @@ k_tiled(const __grid_constant__ CUtensorMap map_src,
     for (int s = 0; s < D; ++s) {
         const float *src = (s & 1) ? sB : sA;
         float *dst = (s & 1) ? sA : sB;
-        const int e = EXACT ? (D - 1 - s) : 0;  // extension beyond the tile
-        const int r0 = max(hy - e, vr0), r1 = min(hy + ty + e, vr1);
-        const int c0 = max(hx - e, vc0), c1 = min(hx + tx + e, vc1);
+        const int r0 = max(hy, vr0), r1 = min(hy + ty, vr1);
+        const int c0 = max(hx, vc0), c1 = min(hx + tx, vc1);
         const bool last = (s == D - 1);
         for (int by = r0 + warp; by < r1; by += nwarps) {
             const float *row = src + by * box_x;
             const float *brow = sBb + by * box_x;
             for (int bx = c0 + lane; bx < c1; bx += 32) {
-                const float v = jacobi_update(row[bx - 1], row[bx + 1],
-                                              row[bx - box_x], row[bx + box_x],
-                                              brow[bx], r, d);
+                const float v = jacobi_update<FAST>(
+                    row[bx - 1], row[bx + 1], row[bx - box_x], row[bx + box_x],
+                    brow[bx], r, d, y);
                 if (last)
                     out[(long long)(byo + by) * ld + (bxo + bx)] = v;
                 else
@@ -164,7 +159,6 @@ k_tiled(const __grid_constant__ CUtensorMap map_src,
     }
 }
 
-template <bool EXACT>
 cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
                          const CUtensorMap *map_src, const CUtensorMap *map_b,
                          float *out, ResidualOut *status,
@@ -173,12 +167,18 @@ cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
                     (g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
     const dim3 block(tc.threads);
 #define TBJ_LAUNCH(DD)                                                        \
-    case DD: {                                                                \
-        k_tiled<DD, EXACT><<<grid, block, tc.smem, stream>>>(                 \
-            *map_src, *map_b, out, g.n, g.ld, g.r, g.d, tc.tile_x, tc.tile_y, \
-            tc.halo_x, tc.halo_y, tc.box_x, tc.box_y, tc.origin, status);     \
-        return cudaGetLastError();                                            \
-    }
+    case DD:                                                                  \
+        if (g.fast)                                                           \
+            k_block_async<DD, true><<<grid, block, tc.smem, stream>>>(        \
+                *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.tile_x,   \
+                tc.tile_y, tc.halo_x, tc.halo_y, tc.box_x, tc.box_y,          \
+                tc.origin, status);                                           \
+        else                                                                  \
+            k_block_async<DD, false><<<grid, block, tc.smem, stream>>>(       \
+                *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.tile_x,   \
+                tc.tile_y, tc.halo_x, tc.halo_y, tc.box_x, tc.box_y,          \
+                tc.origin, status);                                           \
+        return cudaGetLastError();
     switch (tc.depth) {
         TBJ_LAUNCH(1)
         TBJ_LAUNCH(2)
@@ -191,13 +191,17 @@ cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
 #undef TBJ_LAUNCH
 }
 
-template <bool EXACT>
 cudaError_t prepare_tiled(const TileConf &tc) {
 #define TBJ_PREP(DD)                                                          \
-    case DD:                                                                  \
-        return cudaFuncSetAttribute(k_tiled<DD, EXACT>,                       \
+    case DD: {                                                                \
+        cudaError_t e = cudaFuncSetAttribute(                                 \
+            k_block_async<DD, true>,                                          \
+            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc.smem);       \
+        if (e != cudaSuccess) return e;                                       \
+        return cudaFuncSetAttribute(k_block_async<DD, false>,                 \
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                    (int)tc.smem);
+                                    (int)tc.smem);                            \
+    }
     switch (tc.depth) {
         TBJ_PREP(1)
         TBJ_PREP(2)
@@ -221,24 +225,6 @@ int finish_conf(TileConf *tc) {
 
 }  // namespace
 
-int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
-    if (depth != 2 && depth != 4 && depth != 8 && depth != 16) return -1;
-    if (tile_x == 0) tile_x = 128;
-    if (tile_y == 0) tile_y = depth >= 16 ? 64 : 48;
-    if (tile_x < 4 || tile_x % 4 != 0 || tile_y < 1) return -1;
-    (void)n;
-    tc->depth = depth;
-    tc->tile_x = tile_x;
-    tc->tile_y = tile_y;
-    tc->halo_x = (depth + 3) / 4 * 4;
-    tc->halo_y = depth;
-    tc->box_x = tile_x + 2 * tc->halo_x;
-    tc->box_y = tile_y + 2 * depth;
-    tc->origin = 0;
-    tc->threads = 512;
-    return finish_conf(tc);
-}
-
 int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     if (depth != 1 && depth != 2 && depth != 4 && depth != 8 && depth != 16)
         return -1;
@@ -257,29 +243,19 @@ int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->origin = 1;
     const int cells = tile_x * tile_y;
     tc->threads = cells >= 512 ? 512 : (cells + 31) / 32 * 32;
+    tc->variant = 0;
     return finish_conf(tc);
 }
 
-cudaError_t prepare_sweep_etb(const TileConf &tc) {
-    return prepare_tiled<true>(tc);
-}
-
 cudaError_t prepare_sweep_ba(const TileConf &tc) {
-    return prepare_tiled<false>(tc);
-}
-
-cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
-                             const CUtensorMap *map_src,
-                             const CUtensorMap *map_b, float *out,
-                             ResidualOut *status, cudaStream_t stream) {
-    return launch_tiled<true>(g, tc, map_src, map_b, out, status, stream);
+    return prepare_tiled(tc);
 }
 
 cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const CUtensorMap *map_src,
                             const CUtensorMap *map_b, float *out,
                             ResidualOut *status, cudaStream_t stream) {
-    return launch_tiled<false>(g, tc, map_src, map_b, out, status, stream);
+    return launch_tiled(g, tc, map_src, map_b, out, status, stream);
 }
 
 }  // namespace tbj

@@ -21,6 +21,8 @@ STRATEGIES = {"sync": SYNC, "etb": EXACT_TEMPORAL_BLOCKED,
               "exact_temporal_blocked": EXACT_TEMPORAL_BLOCKED,
               "ba": BLOCK_ASYNC, "block_async": BLOCK_ASYNC}
 CONTROLS = {"host": CONTROL_HOST, "device": CONTROL_DEVICE}
+DIVISION_AUTO, DIVISION_IEEE = 0, 1
+DIVISIONS = {"auto": DIVISION_AUTO, "ieee": DIVISION_IEEE}
 
 
 class Config(ctypes.Structure):
@@ -28,7 +30,7 @@ class Config(ctypes.Structure):
                 ("tile_x", ctypes.c_int), ("tile_y", ctypes.c_int),
                 ("check_every", ctypes.c_int), ("tol", ctypes.c_double),
                 ("max_sweeps", ctypes.c_longlong), ("control", ctypes.c_int),
-                ("reserved", ctypes.c_int * 3)]
+                ("division", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
 
 
 class JacobiError(RuntimeError):
@@ -70,6 +72,7 @@ def load():
             "jacobi_set_strategy": (i, [vp, cfgp]),
             "jacobi_run": (ll, [vp, vp, i, ctypes.POINTER(ll)]),
             "jacobi_launch_count": (ll, [vp]),
+            "jacobi_division_mode": (i, [vp]),
             "jacobi_destroy": (None, [vp]),
             "jacobi_last_error": (ctypes.c_char_p, [vp]),
             "jacobi_status_string": (ctypes.c_char_p, [i]),
@@ -110,7 +113,8 @@ def residual_noalloc(u, b, r, norms, stream=None) -> int:
 
 
 def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
-                tol=1e-5, max_sweeps=1 << 22, control="host") -> Config:
+                tol=1e-5, max_sweeps=1 << 22, control="host",
+                division="auto") -> Config:
     c = Config()
     load().jacobi_config_default(ctypes.byref(c))
     c.strategy = STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
@@ -120,6 +124,7 @@ def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
     c.tol = float(tol)
     c.max_sweeps = int(max_sweeps)
     c.control = CONTROLS[control] if isinstance(control, str) else int(control)
+    c.division = DIVISIONS[division] if isinstance(division, str) else int(division)
     return c
 
 
@@ -153,7 +158,7 @@ class Solver:
 
     def __init__(self, u, u_alt, b, r, *, strategy="sync", depth=1,
                  tile=(0, 0), check_every=8, tol=1e-5, max_sweeps=1 << 22,
-                 control="host", stream=None):
+                 control="host", division="auto", stream=None):
         import torch
         lib = load()
         for t in (u, u_alt, b):
@@ -162,7 +167,8 @@ class Solver:
         self.u, self.u_alt, self.b = u, u_alt, b
         self.stream = torch.cuda.current_stream(u.device) if stream is None else stream
         self._h = ctypes.c_void_p()
-        cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps, control)
+        cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
+                          control, division)
         with torch.cuda.device(u.device):
             rc = lib.jacobi_create(ctypes.byref(self._h), self.n, self.ld,
                                    float(r), ctypes.byref(cfg), _ptr(u),
@@ -206,8 +212,10 @@ class Solver:
         return rm.value, bm.value
 
     def set_strategy(self, strategy="sync", depth=1, tile=(0, 0),
-                     check_every=8, tol=1e-5, max_sweeps=1 << 22, control="host"):
-        cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps, control)
+                     check_every=8, tol=1e-5, max_sweeps=1 << 22, control="host",
+                     division="auto"):
+        cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
+                          control, division)
         self._ok(load().jacobi_set_strategy(self.handle, ctypes.byref(cfg)))
         self.config = cfg
 
@@ -219,6 +227,11 @@ class Solver:
         if total < 0:
             self._raise(total)
         return [int(counts[s]) for s in range(steps)]
+
+    @property
+    def division_mode(self) -> int:
+        """1 if the kernels use the verified fixed-divisor division, 0 if IEEE."""
+        return int(self._ok(load().jacobi_division_mode(self.handle)))
 
     @property
     def launch_count(self) -> int:

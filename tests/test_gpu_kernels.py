@@ -39,10 +39,11 @@ def make_solver(u0, r, **kw):
 
 @pytest.mark.parametrize("n", SIZES)
 @pytest.mark.parametrize("pad", [0, 12])
-def test_rhs_sweep_residual_sync(n, pad):
+@pytest.mark.parametrize("division", ["auto", "ieee"])
+def test_rhs_sweep_residual_sync(n, pad, division):
     r = RS[n % len(RS)]
     u0, g = fields(n, pad, seed=n)
-    s, u, b = make_solver(u0, r)
+    s, u, b = make_solver(u0, r, division=division)
     with s:
         s.rhs(to_dev(g))
         b_ref = oracle.rhs(u0, g)
@@ -66,15 +67,24 @@ def test_rhs_sweep_residual_sync(n, pad):
         assert same_bits(np.float32(rm), rm_ref) and same_bits(np.float32(bm), bm_ref)
 
 
-@pytest.mark.parametrize("n", [17, 70, 130, 259, 520])
+# Compiled tile shapes of the exact-temporal-blocking kernel: (default, alternate).
+ETB_TILES = {2: [(0, 0), (248, 60)], 4: [(0, 0), (248, 56)],
+             8: [(0, 0), (240, 48)], 16: [(0, 0), (96, 160)]}
+
+
+@pytest.mark.parametrize("n", [17, 70, 130, 259, 520, 1030])
 @pytest.mark.parametrize("depth", [2, 4, 8, 16])
-@pytest.mark.parametrize("tile", [(0, 0), (32, 8), (64, 24), (4, 1)])
-def test_etb_launch_equals_depth_sync_sweeps(n, depth, tile):
+@pytest.mark.parametrize("alt", [0, 1])
+@pytest.mark.parametrize("division", ["auto", "ieee"])
+def test_etb_launch_equals_depth_sync_sweeps(n, depth, alt, division):
     """Exact temporal blocking: one launch = D synchronous sweeps, bit for
-    bit (section 02, ghost-zone technique)."""
+    bit (section 02, ghost-zone technique), for every compiled tile shape and
+    both division paths."""
     r = 10.0 if depth != 16 else 100.0
+    tile = ETB_TILES[depth][alt]
     u0, g = fields(n, 8, seed=3 * n + depth)
-    s, u, b = make_solver(u0, r, strategy="etb", depth=depth, tile=tile)
+    s, u, b = make_solver(u0, r, strategy="etb", depth=depth, tile=tile,
+                          division=division)
     with s:
         s.rhs(to_dev(g))
         b_ref = oracle.rhs(u0, g)
@@ -109,6 +119,20 @@ def test_block_async_launch_matches_emulator(n, depth, tile):
             assert same_bits(interior(got), interior(ref)), mismatch(got, ref)
         if depth == 1:
             assert same_bits(interior(ref), interior(oracle.sweeps(u0, b_ref, r, 2)))
+
+
+@pytest.mark.parametrize("r", [1.0, 10.0, 100.0])
+def test_fixed_divisor_division_enabled_for_page_couplings(r):
+    """For d = 5, 41, 401 the fixed-divisor division passes its exhaustive
+    check against IEEE division, so the fast path is the one that runs;
+    forcing IEEE division is honoured."""
+    u0, _ = fields(40, 0, seed=2)
+    s, _, _ = make_solver(u0, r)
+    with s:
+        assert s.division_mode == 1
+    s, _, _ = make_solver(u0, r, division="ieee")
+    with s:
+        assert s.division_mode == 0
 
 
 def test_residual_propagates_nan():
