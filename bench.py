@@ -9,7 +9,8 @@ decision), timed with CUDA events on the solver's stream, checks included
 
 Default workload: N = 2048 (ring included), r = 10, Gaussian source
 σ = N/16, amplitude 100, 10 time steps, tol 1e-5, M = 8; strategies SYNC and
-EXACT_TEMPORAL_BLOCKED with D = 2, 4, 8. `value` is the GLUP/s (interior
+EXACT_TEMPORAL_BLOCKED with D = 2, 4, 8; convergence loop on the device
+(--control host: one host round trip per check instead). `value` is the GLUP/s (interior
 points × sweeps ÷ time) of the fastest strategy; every strategy's figures
 are under "strategies". All strategies perform the same sweeps (exact
 temporal blocking is bit-identical to SYNC), so their GLUP/s compare
@@ -211,7 +212,8 @@ def run_ours(args):
         for tok in strategies:
             kw = parse_strategy(tok)
             u.copy_(u0)
-            solvers[tok] = jacobi.Solver(u, u_alt, b, r, stream=stream, **kw)
+            solvers[tok] = jacobi.Solver(u, u_alt, b, r, stream=stream,
+                                         control=args.control, **kw)
 
         def one_step(tok):
             """Reset u⁰ (setup, untimed) and run the ten time steps (timed)."""
@@ -291,6 +293,7 @@ def run_ours(args):
         "config": {"workload": args.workload, "n": n, "r": r, "source": source,
                    "interior_points": interior, "time_steps": TIME_STEPS,
                    "tol": 1e-5, "check_every": 8, "strategy": best,
+                   "control": args.control,
                    "strategies_timed": strategies,
                    "l2": "flushed (512 MiB write) before every timed solve",
                    "parallelism": f"replicas x{world}"},
@@ -457,6 +460,9 @@ def main(argv=None):
     ap.add_argument("--strategies", default=None,
                     help="comma list: sync, etbD, baD, baD@TXxTY (default per workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--control", default="device", choices=["device", "host"],
+                    help="convergence loop on the device (one graph per time "
+                         "step) or on the host (one round trip per check)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-sweeps", type=int, default=0)
     args = ap.parse_args(argv)

@@ -63,9 +63,12 @@ typedef enum {
      * as in section 02 where the reduction's two norms go back to the host. */
     JACOBI_CONTROL_HOST = 0,
     /* The check interval runs inside a device-side conditional WHILE graph
-     * node: the residual kernel sets the loop condition itself, so a whole
-     * time step is one graph launch and one host synchronisation. Same
-     * iterates, same sweep counts as JACOBI_CONTROL_HOST. */
+     * node, so a whole time step is one graph launch and one host
+     * synchronisation. The first launch of each interval also reduces the
+     * residual norms of its input iterate (its first sweep evaluates J(u)
+     * anyway) and its last block applies the stopping rule and sets the loop
+     * condition; launches queued after the stop return at once. Same
+     * iterates, same sweep counts, same statuses as JACOBI_CONTROL_HOST. */
     JACOBI_CONTROL_DEVICE = 1
 } jacobi_control_t;
 

@@ -25,9 +25,12 @@ struct jacobi_handle {
     cudaStream_t capture = nullptr;  // private stream used to record graphs
 
     // Library-owned device scratch.
-    float *partials = nullptr;     // 2 words per residual block
+    float *partials = nullptr;     // 2 words per reduction block
+    size_t partial_blocks = 0;     // capacity of `partials` in blocks
     ResidualOut *dev_out = nullptr;
     ResidualOut *host_out = nullptr;  // pinned
+    LoopState *loop = nullptr;        // device-side loop state
+    LoopState *loop_host = nullptr;   // pinned copy read after each step
 
     // Tiled strategies.
     TileConf tc{};
@@ -38,9 +41,11 @@ struct jacobi_handle {
     long long launches_per_check = 8;
     long long interval = 8;
 
-    // Graph for a check interval starting from u (index 0) and from u_alt
-    // (index 1; only when launches_per_check is odd).
+    // Host control: graph for a check interval starting from u (index 0)
+    // and from u_alt (index 1; only when launches_per_check is odd).
     cudaGraphExec_t batch[2] = {nullptr, nullptr};
+    // Device control: one graph per time step (conditional WHILE loop).
+    cudaGraphExec_t step = nullptr;
     int cur = 0;  // 0: the iterate is in u; 1: in u_alt
 
     long long launches = 0;  // kernels launched so far
@@ -137,9 +142,6 @@ int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
         return fail(h, JACOBI_ERR_INVALID_ARG, "max_sweeps must be >= 1");
     if (c.control != JACOBI_CONTROL_HOST && c.control != JACOBI_CONTROL_DEVICE)
         return fail(h, JACOBI_ERR_INVALID_ARG, "unknown control %d", c.control);
-    if (c.control == JACOBI_CONTROL_DEVICE)
-        return fail(h, JACOBI_ERR_UNSUPPORTED,
-                    "device-side control is not available in this build");
     switch (c.strategy) {
         case JACOBI_SYNC:
             if (c.depth != 1)
@@ -165,22 +167,51 @@ int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     return JACOBI_OK;
 }
 
+// Plain launch control: no stop flag, no fused residual.
+LaunchCtl plain_ctl() {
+    LaunchCtl c;
+    std::memset(&c, 0, sizeof c);
+    return c;
+}
+
+// Control of a launch inside the device-side loop: honours the stop flag;
+// a fused launch also reduces the residual of its input and decides.
+LaunchCtl loop_ctl(jacobi_handle_t *h, bool fused, int src_is_alt,
+                   cudaGraphConditionalHandle cond) {
+    LaunchCtl c = plain_ctl();
+    c.stop = &h->loop->stop;
+    c.fused = fused;
+    c.lp.state = h->loop;
+    c.lp.partials = reinterpret_cast<unsigned *>(h->partials);
+    c.lp.tol = h->cfg.tol;
+    c.lp.max_sweeps = h->cfg.max_sweeps;
+    c.lp.interval = h->interval;
+    c.lp.cond = cond;
+    c.lp.src_is_alt = src_is_alt;
+    return c;
+}
+
 // Enqueue one launch of the configured strategy: src -> dst.
 cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
-                           cudaStream_t s) {
+                           cudaStream_t s, const LaunchCtl &ctl) {
     const float *src = src_is_alt ? h->u_alt : h->u;
     float *dst = src_is_alt ? h->u : h->u_alt;
     const CUtensorMap *map_src = src_is_alt ? &h->map_alt : &h->map_u;
     switch (h->cfg.strategy) {
         case JACOBI_SYNC:
-            return launch_sweep_sync(h->g, src, h->b, dst, s);
+            return launch_sweep_sync(h->g, src, h->b, dst, ctl, s);
         case JACOBI_EXACT_TEMPORAL_BLOCKED:
             return launch_sweep_etb(h->g, h->tc, map_src, &h->map_b, dst,
-                                    h->dev_out, s);
+                                    h->dev_out, ctl, s);
         default:
             return launch_sweep_ba(h->g, h->tc, map_src, &h->map_b, dst,
-                                   h->dev_out, s);
+                                   h->dev_out, ctl, s);
     }
+}
+
+cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
+                           cudaStream_t s) {
+    return enqueue_launch(h, src_is_alt, s, plain_ctl());
 }
 
 void destroy_graphs(jacobi_handle_t *h) {
@@ -188,6 +219,8 @@ void destroy_graphs(jacobi_handle_t *h) {
         if (e) cudaGraphExecDestroy(e);
         e = nullptr;
     }
+    if (h->step) cudaGraphExecDestroy(h->step);
+    h->step = nullptr;
 }
 
 // Record the check interval starting from buffer `start` (0 = u, 1 = u_alt):
@@ -216,6 +249,89 @@ int record_batch(jacobi_handle_t *h, int start, cudaGraphExec_t *exec) {
     if (e != cudaSuccess)
         return fail(h, JACOBI_ERR_CUDA, "recording the check graph: %s",
                     cudaGetErrorString(e));
+    return JACOBI_OK;
+}
+
+// Device control: record the graph of one time step,
+//   reset(LoopState) -> WHILE(cond) { body } -> copy LoopState to the host,
+// where the body is one check interval starting from u (fused first launch,
+// the rest honouring the stop flag); when an interval has an odd number of
+// launches the body holds two intervals so that it starts and ends in u.
+int record_step(jacobi_handle_t *h) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaGraphCreate(&graph, 0);
+    cudaGraphConditionalHandle cond{};
+    cudaGraphNode_t reset_node = nullptr, loop_node = nullptr;
+    size_t count = 1;
+    const long long L = h->launches_per_check;
+    const int halves = (L % 2 == 1) ? 2 : 1;
+    auto check = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+        return e == cudaSuccess;
+    };
+    if (check(e) &&
+        check(cudaGraphConditionalHandleCreate(&cond, graph, 1,
+                                               cudaGraphCondAssignDefault)) &&
+        check(cudaStreamBeginCaptureToGraph(h->capture, graph, nullptr, nullptr,
+                                            0, cudaStreamCaptureModeThreadLocal))) {
+        check(launch_loop_reset(h->loop, h->capture));
+        cudaGraph_t g2 = nullptr;
+        check(cudaStreamEndCapture(h->capture, &g2));
+        check(cudaGraphGetNodes(graph, &reset_node, &count));
+    }
+    cudaGraph_t body = nullptr;
+    if (e == cudaSuccess) {
+        cudaGraphNodeParams p = {};
+        p.type = cudaGraphNodeTypeConditional;
+        p.conditional.handle = cond;
+        p.conditional.type = cudaGraphCondTypeWhile;
+        p.conditional.size = 1;
+        if (check(cudaGraphAddNode(&loop_node, graph, &reset_node, nullptr, 1, &p)))
+            body = p.conditional.phGraph_out[0];
+    }
+    if (e == cudaSuccess &&
+        check(cudaStreamBeginCaptureToGraph(h->capture, body, nullptr, nullptr,
+                                            0, cudaStreamCaptureModeThreadLocal))) {
+        int src = 0;
+        for (int half = 0; half < halves; ++half)
+            for (long long l = 0; l < L; ++l) {
+                check(enqueue_launch(h, src, h->capture,
+                                     loop_ctl(h, l == 0, src, cond)));
+                src ^= 1;
+            }
+        cudaGraph_t g2 = nullptr;
+        check(cudaStreamEndCapture(h->capture, &g2));
+    }
+    if (e == cudaSuccess &&
+        check(cudaStreamBeginCaptureToGraph(h->capture, graph, &loop_node,
+                                            nullptr, 1,
+                                            cudaStreamCaptureModeThreadLocal))) {
+        check(cudaMemcpyAsync(h->loop_host, h->loop, sizeof(LoopState),
+                              cudaMemcpyDeviceToHost, h->capture));
+        cudaGraph_t g2 = nullptr;
+        check(cudaStreamEndCapture(h->capture, &g2));
+    }
+    if (e == cudaSuccess) check(cudaGraphInstantiate(&h->step, graph, 0));
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, JACOBI_ERR_CUDA, "recording the device-loop graph: %s",
+                    cudaGetErrorString(e));
+    }
+    return JACOBI_OK;
+}
+
+// Make sure `partials` holds at least `blocks` reductions' worth of words.
+int ensure_partials(jacobi_handle_t *h, size_t blocks) {
+    if (blocks <= h->partial_blocks) return JACOBI_OK;
+    if (h->partials) {
+        cudaStreamSynchronize(h->stream);
+        cudaFree(h->partials);
+        h->partials = nullptr;
+        h->partial_blocks = 0;
+    }
+    TBJ_CUDA(h, cudaMalloc(&h->partials, sizeof(float) * 2 * blocks));
+    h->partial_blocks = blocks;
     return JACOBI_OK;
 }
 
@@ -293,6 +409,13 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     h->interval = (long long)c.check_every /
                   gcd_ll(c.check_every, h->per_launch) * h->per_launch;
     h->launches_per_check = h->interval / h->per_launch;
+    size_t blocks = (size_t)residual_blocks(h->g);
+    const size_t sweep_blocks = c.strategy == JACOBI_SYNC
+                                    ? (size_t)sweep_sync_blocks(h->g)
+                                    : (size_t)tiled_blocks(h->g, h->tc);
+    if (sweep_blocks > blocks) blocks = sweep_blocks;
+    if ((rc = ensure_partials(h, blocks))) return rc;
+    if (c.control == JACOBI_CONTROL_DEVICE) return record_step(h);
     if ((rc = record_batch(h, 0, &h->batch[0]))) return rc;
     if (h->launches_per_check % 2 == 1)
         if ((rc = record_batch(h, 1, &h->batch[1]))) return rc;
@@ -389,10 +512,11 @@ int jacobi_create(jacobi_handle_t **out, int n, long long ld, float r,
     };
     cudaError_t e;
     if ((e = cudaStreamCreateWithFlags(&h->capture, cudaStreamNonBlocking)) ||
-        (e = cudaMalloc(&h->partials,
-                        sizeof(float) * 2 * (size_t)residual_blocks(h->g))) ||
         (e = cudaMalloc(&h->dev_out, sizeof(ResidualOut))) ||
         (e = cudaMallocHost(&h->host_out, sizeof(ResidualOut))) ||
+        (e = cudaMalloc(&h->loop, sizeof(LoopState))) ||
+        (e = cudaMallocHost(&h->loop_host, sizeof(LoopState))) ||
+        (e = cudaMemsetAsync(h->loop, 0, sizeof(LoopState), h->stream)) ||
         (e = cudaMemsetAsync(h->dev_out, 0, sizeof(ResidualOut), h->stream)) ||
         // Both ping-pong buffers carry the same Dirichlet ring.
         (e = cudaMemcpyAsync(u_alt, u, sizeof(float) * (size_t)n * (size_t)ld,
@@ -402,6 +526,7 @@ int jacobi_create(jacobi_handle_t **out, int n, long long ld, float r,
         return bail(JACOBI_ERR_CUDA);
     }
     std::memset(h->host_out, 0, sizeof(ResidualOut));
+    std::memset(h->loop_host, 0, sizeof(LoopState));
     if ((rc = apply_config(h, c))) return bail(rc);
     *out = h;
     return JACOBI_OK;
@@ -418,8 +543,50 @@ int jacobi_rhs(jacobi_handle_t *h, const float *g) {
     return JACOBI_OK;
 }
 
+// One time step with the device-side loop: one graph launch, one sync.
+static long long solve_step_device(jacobi_handle_t *h) {
+    TBJ_CUDA(h, cudaGraphLaunch(h->step, h->stream));
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    const LoopState st = *h->loop_host;
+    // Launches run (no-ops after the stop included): one body per
+    // iteration; an iteration checks once (twice with two halves).
+    const long long checks = st.result_k / h->interval + 1;
+    const long long per_body = h->launches_per_check % 2 == 1 ? 2 : 1;
+    const long long iters = (checks + per_body - 1) / per_body;
+    h->launches += 1 + iters * per_body * h->launches_per_check;
+    if (!st.stop)
+        return fail(h, JACOBI_ERR_CUDA, "device loop ended without a decision");
+    h->cur = st.where;
+    int rc = settle(h);
+    if (rc) return rc;
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    if (st.err & ERR_TMA_TIMEOUT)
+        return fail(h, JACOBI_ERR_CUDA,
+                    "a TMA load did not complete within its wait limit");
+    switch (st.status) {
+        case 0:
+            return st.result_k;
+        case JACOBI_ERR_NONFINITE:
+            return fail(h, JACOBI_ERR_NONFINITE,
+                        "residual norms not finite (rmax=%g, bmax=%g) after "
+                        "%lld sweeps",
+                        (double)st.rmax, (double)st.bmax, st.result_k);
+        case JACOBI_ERR_NOT_CONVERGED:
+            return fail(h, JACOBI_ERR_NOT_CONVERGED,
+                        "not converged after %lld sweeps (rho=%g)", st.result_k,
+                        st.bmax > 0 ? (double)st.rmax / st.bmax : (double)st.rmax);
+        default:
+            return fail(h, JACOBI_ERR_CUDA, "device loop failed (%d)", st.status);
+    }
+}
+
 long long jacobi_solve_step(jacobi_handle_t *h) {
     if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (h->cfg.control == JACOBI_CONTROL_DEVICE) {
+        int rc = settle(h);
+        if (rc) return rc;
+        return solve_step_device(h);
+    }
     long long k = 0;
     int status = JACOBI_OK;
     for (;;) {
@@ -527,6 +694,8 @@ void jacobi_destroy(jacobi_handle_t *h) {
     if (h->partials) cudaFree(h->partials);
     if (h->dev_out) cudaFree(h->dev_out);
     if (h->host_out) cudaFreeHost(h->host_out);
+    if (h->loop) cudaFree(h->loop);
+    if (h->loop_host) cudaFreeHost(h->loop_host);
     delete h;
 }
 

@@ -88,6 +88,180 @@ struct ResidualOut {
     unsigned ticket;    // last-block counter, returns to 0 after each use
 };
 
+// ---------------------------------------------------------------------------
+// Device-side convergence loop.
+//
+// With JACOBI_CONTROL_DEVICE a whole time step is one graph: a conditional
+// WHILE node repeats the check interval. The first launch of each interval
+// is "fused": besides its sweeps it computes the residual norms of its INPUT
+// iterate (rmax = max d|J(u)-u|, bmax = max |b_I|, exactly as k_residual
+// does, since its first sweep evaluates J(u) anyway), and the last of its
+// blocks to finish applies the stopping rule, updates LoopState and sets the
+// loop condition. Every launch first reads LoopState::stop and returns at
+// once when it is set, so launches queued after the stop do nothing and the
+// answer (the fused launch's input) is left intact.
+// ---------------------------------------------------------------------------
+struct LoopState {
+    float rmax, bmax;     // norms at the last check
+    unsigned err;         // ERR_* bits
+    unsigned ticket;      // last-block counter of the fused reduction
+    long long k;          // sweeps done before the current check interval
+    long long result_k;   // sweep count of the answer once stopped
+    int stop;             // 1 once the step has finished
+    int status;           // 0 converged, or a negative jacobi_status_t
+    int where;            // buffer holding the answer: 0 u, 1 u_alt
+    int pad;
+};
+
+struct LoopParams {
+    LoopState *state;
+    unsigned *partials;      // 2 words per block of the fused launch
+    double tol;
+    long long max_sweeps;
+    long long interval;      // sweeps per check interval
+    cudaGraphConditionalHandle cond;
+    int src_is_alt;          // the fused launch reads u_alt (1) or u (0)
+};
+
+// Per-launch control: stop flag to honour (nullptr: none) and, for a fused
+// launch, where its residual goes.
+struct LaunchCtl {
+    const int *stop;
+    bool fused;
+    LoopParams lp;
+};
+
+__device__ __forceinline__ unsigned warp_max_u(unsigned v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Bit pattern of |x|: non-negative floats order like their bit patterns,
+// and a NaN sorts above +Inf, so maxima of these propagate NaN.
+__device__ __forceinline__ unsigned abs_bits(float x) {
+    return __float_as_uint(fabsf(x));
+}
+
+// Stopping rule at the check of the fused launch's input iterate (run by one
+// thread of the last block). k == 0 is the start of the step: no check there.
+__device__ __forceinline__ void loop_decide(const LoopParams &lp, float rmax,
+                                            float bmax) {
+    LoopState *st = lp.state;
+    st->rmax = rmax;
+    st->bmax = bmax;
+    const long long k = st->k;
+    int stop = 0, status = 0;
+    if (st->err) {
+        stop = 1;
+        status = -2;  // JACOBI_ERR_CUDA
+    } else if (k > 0) {
+        const double rm = (double)rmax, bm = (double)bmax;
+        if (!isfinite(rm) || !isfinite(bm)) {
+            stop = 1;
+            status = -4;  // JACOBI_ERR_NONFINITE
+        } else if (rm == 0.0 || rm < lp.tol * bm) {
+            stop = 1;
+        } else if (k >= lp.max_sweeps) {
+            stop = 1;
+            status = -3;  // JACOBI_ERR_NOT_CONVERGED
+        }
+    }
+    if (stop) {
+        st->status = status;
+        st->where = lp.src_is_alt;
+        st->result_k = k;
+        st->stop = 1;
+    } else {
+        st->k = k + lp.interval;
+    }
+    cudaGraphSetConditional(lp.cond, stop ? 0u : 1u);
+}
+
+// Block-level end of a fused launch: reduce (rm, bm) over the block, publish
+// the block's partials, and let the last block reduce all partials and apply
+// the stopping rule. Every block of a fused launch must call this exactly
+// once (blocks with no cells pass zeros). `scratch` is __shared__ space for
+// 2 * 32 + 1 words.
+__device__ __forceinline__ void fused_block_finish(unsigned rm, unsigned bm,
+                                                   const LoopParams &lp,
+                                                   unsigned *scratch) {
+    const int tid = threadIdx.x + threadIdx.y * blockDim.x;
+    const int nthreads = blockDim.x * blockDim.y;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = (nthreads + 31) >> 5;
+    unsigned *s_r = scratch, *s_b = scratch + 32;
+    unsigned *s_last = scratch + 64;
+    rm = warp_max_u(rm);
+    bm = warp_max_u(bm);
+    __syncthreads();  // scratch may alias memory the block used before
+    if (lane == 0) {
+        s_r[warp] = rm;
+        s_b[warp] = bm;
+    }
+    __syncthreads();
+    const unsigned nblocks = gridDim.x * gridDim.y;
+    const unsigned bid = blockIdx.y * gridDim.x + blockIdx.x;
+    if (tid == 0) {
+        unsigned br = 0u, bb = 0u;
+        for (int w = 0; w < nwarps; ++w) {
+            br = max(br, s_r[w]);
+            bb = max(bb, s_b[w]);
+        }
+        lp.partials[2 * bid] = br;
+        lp.partials[2 * bid + 1] = bb;
+        __threadfence();
+        const unsigned t = atomicAdd(&lp.state->ticket, 1u);
+        *s_last = (t == nblocks - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    rm = 0u;
+    bm = 0u;
+    const volatile unsigned *vp = lp.partials;
+    for (unsigned k = tid; k < nblocks; k += nthreads) {
+        rm = max(rm, vp[2 * k]);
+        bm = max(bm, vp[2 * k + 1]);
+    }
+    rm = warp_max_u(rm);
+    bm = warp_max_u(bm);
+    __syncthreads();
+    if (lane == 0) {
+        s_r[warp] = rm;
+        s_b[warp] = bm;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned br = 0u, bb = 0u;
+        for (int w = 0; w < nwarps; ++w) {
+            br = max(br, s_r[w]);
+            bb = max(bb, s_b[w]);
+        }
+        lp.state->ticket = 0u;
+        loop_decide(lp, __uint_as_float(br), __uint_as_float(bb));
+    }
+}
+
+// Residual contributions of one interior cell (i, x) whose new value nv =
+// J(u) was just computed from centre c and neighbours w, e, n_, s_:
+// e = d|nv - c| and |b_I| with the Dirichlet-ring neighbours folded in.
+__device__ __forceinline__ void cell_residual(float nv, float c, float w,
+                                              float e, float n_, float s_,
+                                              float bb, int i, int x, int n,
+                                              float r, float d, unsigned &rm,
+                                              unsigned &bm) {
+    const float res = __fmul_rn(d, fabsf(__fsub_rn(nv, c)));
+    const float qw = (x - 1 == 0) ? w : 0.f;
+    const float qe = (x + 1 == n - 1) ? e : 0.f;
+    const float qn = (i - 1 == 0) ? n_ : 0.f;
+    const float qs = (i + 1 == n - 1) ? s_ : 0.f;
+    const float q = __fadd_rn(__fadd_rn(qw, qe), __fadd_rn(qn, qs));
+    const float bi = __fadd_rn(bb, __fmul_rn(r, q));
+    rm = max(rm, abs_bits(res));
+    bm = max(bm, abs_bits(bi));
+}
+
 // Launch wrappers (all asynchronous on `stream`). They return the CUDA error
 // of the launch.
 cudaError_t launch_rhs(const GridDesc &g, const float *u, const float *src,
@@ -95,7 +269,10 @@ cudaError_t launch_rhs(const GridDesc &g, const float *u, const float *src,
 cudaError_t launch_copy_interior(const GridDesc &g, const float *src,
                                  float *dst, cudaStream_t stream);
 cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
-                              const float *b, float *out, cudaStream_t stream);
+                              const float *b, float *out,
+                              const LaunchCtl &ctl, cudaStream_t stream);
+int sweep_sync_blocks(const GridDesc &g);
+cudaError_t launch_loop_reset(LoopState *st, cudaStream_t stream);
 // partials: 2 * residual_blocks(g) floats of scratch.
 int residual_blocks(const GridDesc &g);
 cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
@@ -128,7 +305,8 @@ cudaError_t prepare_sweep_etb(const TileConf &tc);
 cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              const CUtensorMap *map_src,
                              const CUtensorMap *map_b, float *out,
-                             ResidualOut *status, cudaStream_t stream);
+                             ResidualOut *status, const LaunchCtl &ctl,
+                             cudaStream_t stream);
 
 // Block-asynchronous sweep (section 02 "Block-asynchronous"): one-cell
 // halo frozen at launch, all tile cells updated D times.
@@ -137,6 +315,9 @@ cudaError_t prepare_sweep_ba(const TileConf &tc);
 cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const CUtensorMap *map_src,
                             const CUtensorMap *map_b, float *out,
-                            ResidualOut *status, cudaStream_t stream);
+                            ResidualOut *status, const LaunchCtl &ctl,
+                            cudaStream_t stream);
+// Blocks of one launch of a tiled strategy (size of the fused partials).
+int tiled_blocks(const GridDesc &g, const TileConf &tc);
 
 }  // namespace tbj

@@ -115,12 +115,13 @@ __device__ __forceinline__ float4 hold4(float4 nv, float4 old, bool row_ok,
     return o;
 }
 
-template <int D, int CH, int RW, int NW, bool FAST, bool EDGE>
+template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool FUSED>
 __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
                                            const float4 (&breg)[RW][CH],
                                            float *__restrict__ out, int n,
                                            long long ld, float r, float d,
-                                           float y, int bxo, int byo) {
+                                           float y, int bxo, int byo,
+                                           unsigned &rm, unsigned &bm) {
     using S = EtbShape<D, CH, RW, NW>;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -178,6 +179,29 @@ __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
                     const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
                     float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w,
                                               e, r, d, y);
+                    if (FUSED && s == 0 && in_tile[c] && row >= D &&
+                        row < D + S::TY && row_ok) {
+                        // Residual of the launch's input at the tile's cells.
+                        const float4 c4 = cr[c], n4 = nr[c], s4 = sr[c];
+                        const float4 b4 = breg[j][c];
+                        if (EDGE) {
+                            const int gx = bxo + 128 * c + 4 * lane;
+                            if (colmask[c] & 1u) cell_residual(nv.x, c4.x, w, c4.y, n4.x, s4.x, b4.x, gy, gx + 0, n, r, d, rm, bm);
+                            if (colmask[c] & 2u) cell_residual(nv.y, c4.y, c4.x, c4.z, n4.y, s4.y, b4.y, gy, gx + 1, n, r, d, rm, bm);
+                            if (colmask[c] & 4u) cell_residual(nv.z, c4.z, c4.y, c4.w, n4.z, s4.z, b4.z, gy, gx + 2, n, r, d, rm, bm);
+                            if (colmask[c] & 8u) cell_residual(nv.w, c4.w, c4.z, e, n4.w, s4.w, b4.w, gy, gx + 3, n, r, d, rm, bm);
+                        } else {
+                            // No ring cell is next to these cells: b_I = b.
+                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.x, c4.x)))));
+                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.y, c4.y)))));
+                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.z, c4.z)))));
+                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.w, c4.w)))));
+                            bm = max(bm, abs_bits(b4.x));
+                            bm = max(bm, abs_bits(b4.y));
+                            bm = max(bm, abs_bits(b4.z));
+                            bm = max(bm, abs_bits(b4.w));
+                        }
+                    }
                     if (EDGE) nv = hold4(nv, cr[c], row_ok, colmask[c]);
                     if (!last) {
                         sts4(dst + row * S::BX + 128 * c + 4 * lane, nv);
@@ -201,16 +225,22 @@ __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
     }
 }
 
-template <int D, int CH, int RW, int NW, bool FAST>
+template <int D, int CH, int RW, int NW, bool FAST, bool FUSED>
 __global__ void __launch_bounds__(32 * NW)
 k_etb(const __grid_constant__ CUtensorMap map_src,
       const __grid_constant__ CUtensorMap map_b, float *__restrict__ out,
-      int n, long long ld, float r, float d, float y, ResidualOut *status) {
+      int n, long long ld, float r, float d, float y, unsigned *err,
+      const int *stop, LoopParams lp) {
     using S = EtbShape<D, CH, RW, NW>;
+    if (stop && *stop) return;  // same value for every thread of the launch
+    __shared__ unsigned fin_scratch[65];
     const int gx0 = blockIdx.x * S::TX;  // tile's first cell (grid coords)
     const int gy0 = blockIdx.y * S::TY;
-    if (gx0 > n - 2 || gy0 > n - 2) return;  // tile holds no interior cell
-    const int bxo = gx0 - S::HX;             // grid coords of box cell (0,0)
+    if (gx0 > n - 2 || gy0 > n - 2) {  // tile holds no interior cell
+        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
+        return;
+    }
+    const int bxo = gx0 - S::HX;  // grid coords of box cell (0,0)
     const int byo = gy0 - D;
 
     extern __shared__ unsigned char smem_raw[];
@@ -236,8 +266,9 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
     __syncthreads();
     const bool ok = mbar_wait_bounded(bar);
     if (__syncthreads_or(!ok)) {
-        if (tid == 0) atomicOr(&status->err, (unsigned)ERR_TMA_TIMEOUT);
+        if (tid == 0) atomicOr(err, (unsigned)ERR_TMA_TIMEOUT);
         mbar_wait_bounded(bar);
+        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
         return;
     }
     // b of this warp's band into registers; then the B buffer is free.
@@ -251,14 +282,16 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
             breg[j][c] = lds4(sB + (band + j) * S::BX + 128 * c + 4 * lane);
     __syncthreads();
 
+    unsigned rm = 0u, bm = 0u;
     const bool edge = bxo < 1 || byo < 1 || bxo + S::BX > n - 1 ||
                       byo + S::BY > n - 1;
     if (edge)
-        etb_sweeps<D, CH, RW, NW, FAST, true>(sA, sB, breg, out, n, ld, r, d, y,
-                                              bxo, byo);
+        etb_sweeps<D, CH, RW, NW, FAST, true, FUSED>(sA, sB, breg, out, n, ld, r,
+                                                     d, y, bxo, byo, rm, bm);
     else
-        etb_sweeps<D, CH, RW, NW, FAST, false>(sA, sB, breg, out, n, ld, r, d,
-                                               y, bxo, byo);
+        etb_sweeps<D, CH, RW, NW, FAST, false, FUSED>(sA, sB, breg, out, n, ld,
+                                                      r, d, y, bxo, byo, rm, bm);
+    if (FUSED) fused_block_finish(rm, bm, lp, fin_scratch);
 }
 
 // Shapes per depth: {CH, RW, NW}. Index 0 is the default.
@@ -275,28 +308,38 @@ constexpr EtbVariant kVariants[] = {
 template <int D, int CH, int RW, int NW>
 cudaError_t launch_variant(const GridDesc &g, const CUtensorMap *map_src,
                            const CUtensorMap *map_b, float *out,
-                           ResidualOut *status, cudaStream_t stream) {
+                           unsigned *err, const LaunchCtl &ctl,
+                           cudaStream_t stream) {
     using S = EtbShape<D, CH, RW, NW>;
     const dim3 grid((g.n + S::TX - 1) / S::TX, (g.n + S::TY - 1) / S::TY);
-    if (g.fast)
-        k_etb<D, CH, RW, NW, true><<<grid, 32 * NW, S::SMEM, stream>>>(
-            *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, status);
-    else
-        k_etb<D, CH, RW, NW, false><<<grid, 32 * NW, S::SMEM, stream>>>(
-            *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, status);
+#define TBJ_K(F, FU)                                                          \
+    k_etb<D, CH, RW, NW, F, FU><<<grid, 32 * NW, S::SMEM, stream>>>(          \
+        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, err, ctl.stop, ctl.lp)
+    if (g.fast) {
+        if (ctl.fused) TBJ_K(true, true);
+        else TBJ_K(true, false);
+    } else {
+        if (ctl.fused) TBJ_K(false, true);
+        else TBJ_K(false, false);
+    }
+#undef TBJ_K
     return cudaGetLastError();
 }
 
 template <int D, int CH, int RW, int NW>
 cudaError_t prepare_variant() {
     using S = EtbShape<D, CH, RW, NW>;
-    cudaError_t e = cudaFuncSetAttribute(k_etb<D, CH, RW, NW, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)S::SMEM);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_etb<D, CH, RW, NW, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)S::SMEM);
+    const void *kernels[4] = {
+        (const void *)k_etb<D, CH, RW, NW, true, false>,
+        (const void *)k_etb<D, CH, RW, NW, false, false>,
+        (const void *)k_etb<D, CH, RW, NW, true, true>,
+        (const void *)k_etb<D, CH, RW, NW, false, true>};
+    for (const void *k : kernels) {
+        cudaError_t e = cudaFuncSetAttribute(
+            k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Dispatch on a variant index (into kVariants).
@@ -358,11 +401,13 @@ cudaError_t prepare_sweep_etb(const TileConf &tc) {
 cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              const CUtensorMap *map_src,
                              const CUtensorMap *map_b, float *out,
-                             ResidualOut *status, cudaStream_t stream) {
+                             ResidualOut *status, const LaunchCtl &ctl,
+                             cudaStream_t stream) {
+    unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
     switch (tc.variant) {
 #define TBJ_LAUNCH(I, D, CH, RW, NW) \
     case I:                          \
-        return launch_variant<D, CH, RW, NW>(g, map_src, map_b, out, status, stream);
+        return launch_variant<D, CH, RW, NW>(g, map_src, map_b, out, err, ctl, stream);
         TBJ_ETB_VARIANTS(TBJ_LAUNCH)
 #undef TBJ_LAUNCH
         default:

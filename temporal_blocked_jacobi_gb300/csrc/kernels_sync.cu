@@ -76,42 +76,62 @@ __device__ __forceinline__ RowIn load_row(const float *__restrict__ u,
 
 // ---------------------------------------------------------------------------
 // Synchronous sweep u -> out (section 02 "Synchronous"): every interior cell
-// gets J(u); the ring of out is never written.
+// gets J(u); the ring of out is never written. FUSED also reduces the
+// residual norms of the input u (see LoopState); `stop`, when given, makes
+// the launch a no-op once the device-side loop has stopped.
 // ---------------------------------------------------------------------------
-template <int ROWS, bool FAST>
+template <int ROWS, bool FAST, bool FUSED>
 __global__ void __launch_bounds__(32 * kWarps)
 k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
              float *__restrict__ out, int n, long long ld, float r, float d,
-             float y) {
+             float y, const int *stop, LoopParams lp) {
+    if (stop && *stop) return;  // same value for every thread of the launch
     const int lane = threadIdx.x;
     const int vx = blockIdx.x * 32 + lane;
     const int x0 = vx * 4;
     const bool active = x0 < n;
     const int i0 = 1 + (blockIdx.y * kWarps + threadIdx.y) * ROWS;
-    if (i0 > n - 2) return;  // uniform across the warp
     const int i1 = min(i0 + ROWS, n - 1);
-
-    float4 top = make_float4(0.f, 0.f, 0.f, 0.f), mid = top;
-    if (active) {
-        top = ld4(u + (long long)(i0 - 1) * ld + x0);
-        mid = ld4(u + (long long)i0 * ld + x0);
+    unsigned rm = 0u, bm = 0u;
+    if (i0 <= n - 2) {  // uniform across the warp
+        float4 top = make_float4(0.f, 0.f, 0.f, 0.f), mid = top;
+        if (active) {
+            top = ld4(u + (long long)(i0 - 1) * ld + x0);
+            mid = ld4(u + (long long)i0 * ld + x0);
+        }
+        RowIn next = load_row(u, b, ld, n, i0, x0, lane, active);
+        for (int i = i0; i < i1; ++i) {
+            const RowIn cur = next;
+            if (i + 1 < i1) next = load_row(u, b, ld, n, i + 1, x0, lane, active);
+            float west = __shfl_up_sync(FULL, mid.w, 1);
+            float east = __shfl_down_sync(FULL, mid.x, 1);
+            if (lane == 0) west = cur.edge;
+            if (lane == 31) east = cur.edge;
+            float4 o;
+            o.x = jacobi_update<FAST>(west, mid.y, top.x, cur.bot.x, cur.bb.x, r, d, y);
+            o.y = jacobi_update<FAST>(mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, r, d, y);
+            o.z = jacobi_update<FAST>(mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, r, d, y);
+            o.w = jacobi_update<FAST>(mid.z, east, top.w, cur.bot.w, cur.bb.w, r, d, y);
+            if (active) {
+                store_interior(out + (long long)i * ld, x0, n, o);
+                if (FUSED) {
+                    if (x0 + 0 >= 1 && x0 + 0 <= n - 2)
+                        cell_residual(o.x, mid.x, west, mid.y, top.x, cur.bot.x, cur.bb.x, i, x0 + 0, n, r, d, rm, bm);
+                    if (x0 + 1 >= 1 && x0 + 1 <= n - 2)
+                        cell_residual(o.y, mid.y, mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, i, x0 + 1, n, r, d, rm, bm);
+                    if (x0 + 2 >= 1 && x0 + 2 <= n - 2)
+                        cell_residual(o.z, mid.z, mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, i, x0 + 2, n, r, d, rm, bm);
+                    if (x0 + 3 >= 1 && x0 + 3 <= n - 2)
+                        cell_residual(o.w, mid.w, mid.z, east, top.w, cur.bot.w, cur.bb.w, i, x0 + 3, n, r, d, rm, bm);
+                }
+            }
+            top = mid;
+            mid = cur.bot;
+        }
     }
-    RowIn next = load_row(u, b, ld, n, i0, x0, lane, active);
-    for (int i = i0; i < i1; ++i) {
-        const RowIn cur = next;
-        if (i + 1 < i1) next = load_row(u, b, ld, n, i + 1, x0, lane, active);
-        float west = __shfl_up_sync(FULL, mid.w, 1);
-        float east = __shfl_down_sync(FULL, mid.x, 1);
-        if (lane == 0) west = cur.edge;
-        if (lane == 31) east = cur.edge;
-        float4 o;
-        o.x = jacobi_update<FAST>(west, mid.y, top.x, cur.bot.x, cur.bb.x, r, d, y);
-        o.y = jacobi_update<FAST>(mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, r, d, y);
-        o.z = jacobi_update<FAST>(mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, r, d, y);
-        o.w = jacobi_update<FAST>(mid.z, east, top.w, cur.bot.w, cur.bb.w, r, d, y);
-        if (active) store_interior(out + (long long)i * ld, x0, n, o);
-        top = mid;
-        mid = cur.bot;
+    if (FUSED) {
+        __shared__ unsigned scratch[65];
+        fused_block_finish(rm, bm, lp, scratch);
     }
 }
 
@@ -280,6 +300,18 @@ __global__ void k_copy_interior(const float *__restrict__ src,
     }
 }
 
+__global__ void k_loop_reset(LoopState *st) {
+    st->rmax = 0.f;
+    st->bmax = 0.f;
+    st->err = 0u;
+    st->ticket = 0u;
+    st->k = 0;
+    st->result_k = 0;
+    st->stop = 0;
+    st->status = 0;
+    st->where = 0;
+}
+
 dim3 strip_grid(int n, int rows) {
     const int nvec = (n + 3) / 4;
     const int per_block = kWarps * rows;
@@ -309,28 +341,42 @@ cudaError_t launch_copy_interior(const GridDesc &g, const float *src,
 }
 
 cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
-                              const float *b, float *out,
+                              const float *b, float *out, const LaunchCtl &ctl,
                               cudaStream_t stream) {
     const int rows = rows_per_warp(g.n);
     const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
-#define TBJ_SWEEP(R)                                                           \
-    case R:                                                                    \
-        if (g.fast)                                                            \
-            k_sweep_sync<R, true><<<grid, block, 0, stream>>>(u, b, out, g.n,  \
-                                                              g.ld, g.r, g.d,  \
-                                                              g.y);            \
-        else                                                                   \
-            k_sweep_sync<R, false><<<grid, block, 0, stream>>>(u, b, out, g.n, \
-                                                               g.ld, g.r, g.d, \
-                                                               g.y);           \
+#define TBJ_SWEEP(R, F, FU)                                                   \
+    k_sweep_sync<R, F, FU><<<grid, block, 0, stream>>>(u, b, out, g.n, g.ld,  \
+                                                       g.r, g.d, g.y,         \
+                                                       ctl.stop, ctl.lp)
+#define TBJ_SWEEP_R(R)                                                        \
+    case R:                                                                   \
+        if (g.fast) {                                                         \
+            if (ctl.fused) TBJ_SWEEP(R, true, true);                          \
+            else TBJ_SWEEP(R, true, false);                                   \
+        } else {                                                              \
+            if (ctl.fused) TBJ_SWEEP(R, false, true);                         \
+            else TBJ_SWEEP(R, false, false);                                  \
+        }                                                                     \
         break;
     switch (rows) {
-        TBJ_SWEEP(4)
-        TBJ_SWEEP(8)
-        TBJ_SWEEP(16)
-        TBJ_SWEEP(32)
+        TBJ_SWEEP_R(4)
+        TBJ_SWEEP_R(8)
+        TBJ_SWEEP_R(16)
+        TBJ_SWEEP_R(32)
     }
+#undef TBJ_SWEEP_R
 #undef TBJ_SWEEP
+    return cudaGetLastError();
+}
+
+int sweep_sync_blocks(const GridDesc &g) {
+    const dim3 grid = strip_grid(g.n, rows_per_warp(g.n));
+    return (int)(grid.x * grid.y);
+}
+
+cudaError_t launch_loop_reset(LoopState *st, cudaStream_t stream) {
+    k_loop_reset<<<1, 1, 0, stream>>>(st);
     return cudaGetLastError();
 }
 

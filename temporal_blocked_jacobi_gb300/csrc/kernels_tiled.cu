@@ -88,16 +88,21 @@ __host__ __device__ inline size_t buffer_bytes(int box_x, int box_y) {
     return round128((size_t)box_x * box_y * sizeof(float));
 }
 
-template <int D, bool FAST>
+template <int D, bool FAST, bool FUSED>
 __global__ void __launch_bounds__(512)
 k_block_async(const __grid_constant__ CUtensorMap map_src,
               const __grid_constant__ CUtensorMap map_b,
               float *__restrict__ out, int n, long long ld, float r, float d,
               float y, int tx, int ty, int hx, int hy, int box_x, int box_y,
-              int origin, ResidualOut *status) {
+              int origin, unsigned *err, const int *stop, LoopParams lp) {
+    if (stop && *stop) return;  // same value for every thread of the launch
+    __shared__ unsigned fin_scratch[65];
     const int gx0 = origin + blockIdx.x * tx;  // tile's first cell (grid)
     const int gy0 = origin + blockIdx.y * ty;
-    if (gx0 > n - 2 || gy0 > n - 2 || gx0 + tx <= 1 || gy0 + ty <= 1) return;
+    if (gx0 > n - 2 || gy0 > n - 2 || gx0 + tx <= 1 || gy0 + ty <= 1) {
+        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
+        return;
+    }
     const int bxo = gx0 - hx;  // grid coordinates of box cell (0, 0)
     const int byo = gy0 - hy;
 
@@ -122,10 +127,11 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
     __syncthreads();
     const bool ok = mbar_wait_bounded(bar);
     if (__syncthreads_or(!ok)) {
-        if (tid == 0) atomicOr(&status->err, (unsigned)ERR_TMA_TIMEOUT);
+        if (tid == 0) atomicOr(err, (unsigned)ERR_TMA_TIMEOUT);
         // Let any copy still in flight land before the block's shared
         // memory is released (bounded as well).
         mbar_wait_bounded(bar);
+        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
         return;
     }
 
@@ -135,6 +141,7 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
     const int warp = tid >> 5, lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
 
+    unsigned rm = 0u, bm = 0u;
 #pragma unroll 1
     for (int s = 0; s < D; ++s) {
         const float *src = (s & 1) ? sB : sA;
@@ -146,9 +153,12 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
             const float *row = src + by * box_x;
             const float *brow = sBb + by * box_x;
             for (int bx = c0 + lane; bx < c1; bx += 32) {
-                const float v = jacobi_update<FAST>(
-                    row[bx - 1], row[bx + 1], row[bx - box_x], row[bx + box_x],
-                    brow[bx], r, d, y);
+                const float w = row[bx - 1], e = row[bx + 1];
+                const float nn = row[bx - box_x], ss = row[bx + box_x];
+                const float v = jacobi_update<FAST>(w, e, nn, ss, brow[bx], r, d, y);
+                if (FUSED && s == 0)  // residual of the launch's input
+                    cell_residual(v, row[bx], w, e, nn, ss, brow[bx], byo + by,
+                                  bxo + bx, n, r, d, rm, bm);
                 if (last)
                     out[(long long)(byo + by) * ld + (bxo + bx)] = v;
                 else
@@ -157,27 +167,30 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
         }
         if (!last) __syncthreads();
     }
+    if (FUSED) fused_block_finish(rm, bm, lp, fin_scratch);
 }
 
 cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
                          const CUtensorMap *map_src, const CUtensorMap *map_b,
-                         float *out, ResidualOut *status,
+                         float *out, unsigned *err, const LaunchCtl &ctl,
                          cudaStream_t stream) {
     const dim3 grid((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x,
                     (g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
     const dim3 block(tc.threads);
+#define TBJ_K(DD, F, FU)                                                      \
+    k_block_async<DD, F, FU><<<grid, block, tc.smem, stream>>>(               \
+        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.tile_x,           \
+        tc.tile_y, tc.halo_x, tc.halo_y, tc.box_x, tc.box_y, tc.origin, err,  \
+        ctl.stop, ctl.lp)
 #define TBJ_LAUNCH(DD)                                                        \
     case DD:                                                                  \
-        if (g.fast)                                                           \
-            k_block_async<DD, true><<<grid, block, tc.smem, stream>>>(        \
-                *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.tile_x,   \
-                tc.tile_y, tc.halo_x, tc.halo_y, tc.box_x, tc.box_y,          \
-                tc.origin, status);                                           \
-        else                                                                  \
-            k_block_async<DD, false><<<grid, block, tc.smem, stream>>>(       \
-                *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.tile_x,   \
-                tc.tile_y, tc.halo_x, tc.halo_y, tc.box_x, tc.box_y,          \
-                tc.origin, status);                                           \
+        if (g.fast) {                                                         \
+            if (ctl.fused) TBJ_K(DD, true, true);                             \
+            else TBJ_K(DD, true, false);                                      \
+        } else {                                                              \
+            if (ctl.fused) TBJ_K(DD, false, true);                            \
+            else TBJ_K(DD, false, false);                                     \
+        }                                                                     \
         return cudaGetLastError();
     switch (tc.depth) {
         TBJ_LAUNCH(1)
@@ -189,29 +202,32 @@ cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
             return cudaErrorInvalidValue;
     }
 #undef TBJ_LAUNCH
+#undef TBJ_K
+}
+
+template <int DD>
+cudaError_t prepare_depth(size_t smem) {
+    const void *kernels[4] = {(const void *)k_block_async<DD, true, false>,
+                              (const void *)k_block_async<DD, false, false>,
+                              (const void *)k_block_async<DD, true, true>,
+                              (const void *)k_block_async<DD, false, true>};
+    for (const void *k : kernels) {
+        cudaError_t e = cudaFuncSetAttribute(
+            k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t prepare_tiled(const TileConf &tc) {
-#define TBJ_PREP(DD)                                                          \
-    case DD: {                                                                \
-        cudaError_t e = cudaFuncSetAttribute(                                 \
-            k_block_async<DD, true>,                                          \
-            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc.smem);       \
-        if (e != cudaSuccess) return e;                                       \
-        return cudaFuncSetAttribute(k_block_async<DD, false>,                 \
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                    (int)tc.smem);                            \
-    }
     switch (tc.depth) {
-        TBJ_PREP(1)
-        TBJ_PREP(2)
-        TBJ_PREP(4)
-        TBJ_PREP(8)
-        TBJ_PREP(16)
-        default:
-            return cudaErrorInvalidValue;
+        case 1: return prepare_depth<1>(tc.smem);
+        case 2: return prepare_depth<2>(tc.smem);
+        case 4: return prepare_depth<4>(tc.smem);
+        case 8: return prepare_depth<8>(tc.smem);
+        case 16: return prepare_depth<16>(tc.smem);
+        default: return cudaErrorInvalidValue;
     }
-#undef TBJ_PREP
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;
@@ -254,8 +270,15 @@ cudaError_t prepare_sweep_ba(const TileConf &tc) {
 cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const CUtensorMap *map_src,
                             const CUtensorMap *map_b, float *out,
-                            ResidualOut *status, cudaStream_t stream) {
-    return launch_tiled(g, tc, map_src, map_b, out, status, stream);
+                            ResidualOut *status, const LaunchCtl &ctl,
+                            cudaStream_t stream) {
+    unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
+    return launch_tiled(g, tc, map_src, map_b, out, err, ctl, stream);
+}
+
+int tiled_blocks(const GridDesc &g, const TileConf &tc) {
+    return ((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x) *
+           ((g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
 }
 
 }  // namespace tbj

@@ -62,19 +62,27 @@ def test_host_buffers_rejected():
     assert not h.value
 
 
-def test_sweep_cap_not_converged_then_recovers():
+@pytest.mark.parametrize("control", ["host", "device"])
+@pytest.mark.parametrize("strategy,depth", [("sync", 1), ("etb", 8), ("ba", 4)])
+def test_sweep_cap_not_converged_then_recovers(control, strategy, depth):
     import torch
+    import oracle
     jacobi = _jacobi()
     n, r = 128, 100.0
     u0, g = workload(n, "point")
     u, u_alt, b = jacobi.allocate(n, u0.shape[1])
     u.copy_(to_dev(u0))
-    with jacobi.Solver(u, u_alt, b, r, max_sweeps=24) as s:
+    with jacobi.Solver(u, u_alt, b, r, max_sweeps=24, strategy=strategy,
+                       depth=depth, control=control) as s:
         s.rhs(to_dev(g))
         k = s.solve_step(raise_on_error=False)
         assert k == jacobi.ERR_NOT_CONVERGED
         assert "not converged" in s.last_error
-        s.set_strategy("sync", 1, max_sweeps=1 << 22)
+        # u holds the iterate at the cap (24 sweeps), as the oracle's does
+        if strategy != "ba":
+            ref = oracle.sweeps(u0, oracle.rhs(u0, g), r, 24)
+            assert np.array_equal(u.cpu().numpy(), ref)
+        s.set_strategy(strategy, depth, max_sweeps=1 << 22, control=control)
         assert s.solve_step() > 0
     torch.cuda.synchronize()
 
@@ -86,21 +94,24 @@ def test_nan_source_reports_nonfinite():
     g[10, 12] = np.nan
     u, u_alt, b = jacobi.allocate(n, u0.shape[1])
     u.copy_(to_dev(u0))
-    for kw in ({}, {"strategy": "etb", "depth": 4}, {"strategy": "ba", "depth": 2}):
+    for kw in ({}, {"strategy": "etb", "depth": 4}, {"strategy": "ba", "depth": 2},
+               {"control": "device"}, {"strategy": "etb", "depth": 8, "control": "device"},
+               {"strategy": "ba", "depth": 2, "control": "device"}):
         u.copy_(to_dev(u0))
         with jacobi.Solver(u, u_alt, b, 1.0, **kw) as s:
             s.rhs(to_dev(g))
             assert s.solve_step(raise_on_error=False) == jacobi.ERR_NONFINITE
 
 
-def test_zero_problem_converges_at_first_check():
+@pytest.mark.parametrize("control", ["host", "device"])
+def test_zero_problem_converges_at_first_check(control):
     jacobi = _jacobi()
     n = 50
     u0 = P.initial_field(n, top=0.0)
     g = P.source_term(n, kind="zero")
     u, u_alt, b = jacobi.allocate(n, u0.shape[1])
     u.copy_(to_dev(u0))
-    with jacobi.Solver(u, u_alt, b, 10.0, strategy="etb", depth=8) as s:
+    with jacobi.Solver(u, u_alt, b, 10.0, strategy="etb", depth=8, control=control) as s:
         s.rhs(to_dev(g))
         assert s.solve_step() == 8
         assert s.residual() == (0.0, 0.0)
@@ -118,3 +129,26 @@ def test_launch_count_grows():
         k = s.solve_step()
         # rhs + k sweeps + one residual per check interval of 8
         assert s.launch_count - c0 == 1 + k + k // 8
+
+
+@pytest.mark.parametrize("strategy,depth", [("sync", 1), ("etb", 4), ("etb", 8)])
+def test_device_control_launch_count(strategy, depth):
+    """Device control: one graph per step holding a reset kernel and the loop
+    body; launches after the stop are counted (they run and return)."""
+    jacobi = _jacobi()
+    n = 64
+    u0, g = workload(n, "point")
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    with jacobi.Solver(u, u_alt, b, 10.0, strategy=strategy, depth=depth,
+                       control="device") as s:
+        s.rhs(to_dev(g))
+        c0 = s.launch_count
+        k = s.solve_step()
+        per = 1 if strategy == "sync" else depth
+        L = 8 // per if per <= 8 else 1
+        checks = k // 8 + 1
+        body = 2 if L % 2 else 1
+        iters = -(-checks // body)
+        copy = 1 if (L % 2 and checks % 2 == 0) else 0
+        assert s.launch_count - c0 == 1 + iters * body * L + copy

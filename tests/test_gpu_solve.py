@@ -22,10 +22,14 @@ from tests.gpu_helpers import gpu_run, interior, mismatch, same_bits, to_dev, wo
 pytestmark = pytest.mark.gpu
 
 
-def test_n512_r1_point_sync_bit_exact():
+CONTROLS = ["host", "device"]
+
+
+@pytest.mark.parametrize("control", CONTROLS)
+def test_n512_r1_point_sync_bit_exact(control):
     u0, g = workload(512, "point")
     ref_u, ref_k, _ = oracle.run(u0, g, 1.0)
-    got_u, got_k, _ = gpu_run(u0, g, 1.0)
+    got_u, got_k, _ = gpu_run(u0, g, 1.0, control=control)
     assert got_k == ref_k
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
 
@@ -37,25 +41,29 @@ def n2048_reference():
     return u0, g, ref_u, ref_k
 
 
+@pytest.mark.parametrize("control", CONTROLS)
 @pytest.mark.parametrize("strategy,depth", [("sync", 1), ("etb", 2), ("etb", 4), ("etb", 8)])
-def test_n2048_r10_gauss_bit_exact(n2048_reference, strategy, depth):
+def test_n2048_r10_gauss_bit_exact(n2048_reference, strategy, depth, control):
     u0, g, ref_u, ref_k = n2048_reference
-    got_u, got_k, _ = gpu_run(u0, g, 10.0, strategy=strategy, depth=depth)
+    got_u, got_k, _ = gpu_run(u0, g, 10.0, strategy=strategy, depth=depth,
+                              control=control)
     assert got_k == ref_k
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
 
 
+@pytest.mark.parametrize("control", CONTROLS)
 @pytest.mark.parametrize("n,r,source", [(130, 100.0, "gauss"), (70, 10.0, "point")])
-def test_etb16_checks_every_16_sweeps(n, r, source):
+def test_etb16_checks_every_16_sweeps(n, r, source, control):
     """A 16-sweep launch is checked every lcm(8, 16) = 16 sweeps; it equals
     synchronous sweeps checked every 16."""
     u0, g = workload(n, source)
     ref_u, ref_k, _ = oracle.run(u0, g, r, m=16)
-    got_u, got_k, _ = gpu_run(u0, g, r, strategy="etb", depth=16)
+    got_u, got_k, _ = gpu_run(u0, g, r, strategy="etb", depth=16, control=control)
     assert got_k == ref_k and all(k % 16 == 0 for k in got_k)
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
 
 
+@pytest.mark.parametrize("control", CONTROLS)
 @pytest.mark.parametrize("n,r,source,depth,tile", [
     (256, 10.0, "point", 4, (32, 8)),
     (256, 1.0, "gauss", 2, (32, 8)),
@@ -63,10 +71,11 @@ def test_etb16_checks_every_16_sweeps(n, r, source):
     (258, 10.0, "point", 8, (32, 16)),
     (130, 10.0, "gauss", 16, (128, 64)),
 ])
-def test_block_async_solve(n, r, source, depth, tile):
+def test_block_async_solve(n, r, source, depth, tile, control):
     u0, g = workload(n, source)
     ref_u, ref_k, _ = oracle.run(u0, g, r, depth=depth, tile_x=tile[0], tile_y=tile[1])
-    got_u, got_k, got_b = gpu_run(u0, g, r, strategy="ba", depth=depth, tile=tile)
+    got_u, got_k, got_b = gpu_run(u0, g, r, strategy="ba", depth=depth, tile=tile,
+                                  control=control)
     assert got_k == ref_k
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
     # within 5e-4 ||b||inf of the synchronous answer
@@ -95,9 +104,10 @@ def test_strategy_change_between_steps():
     g_dev = to_dev(g)
     counts = []
     with jacobi.Solver(u, u_alt, b, r) as s:
-        for step, (strategy, depth) in enumerate(
-                [("sync", 1), ("etb", 4), ("etb", 8), ("sync", 1), ("etb", 2), ("etb", 8)]):
-            s.set_strategy(strategy, depth)
+        for step, (strategy, depth, control) in enumerate(
+                [("sync", 1, "host"), ("etb", 4, "device"), ("etb", 8, "device"),
+                 ("sync", 1, "device"), ("etb", 2, "host"), ("etb", 8, "host")]):
+            s.set_strategy(strategy, depth, control=control)
             s.rhs(g_dev)
             counts.append(s.solve_step())
     torch.cuda.synchronize()
@@ -110,7 +120,7 @@ def test_mirror_symmetry_on_gpu():
     c = (n - 1) / 2
     u0 = P.initial_field(n, 68)
     g = P.source_term(n, 68, "gauss", center=(c, c))
-    for kw in ({}, {"strategy": "etb", "depth": 8}):
+    for kw in ({}, {"strategy": "etb", "depth": 8}, {"control": "device"}):
         got_u, _, _ = gpu_run(u0, g, 100.0, **kw)
         inner = got_u[:, :n]
         assert same_bits(inner, inner[:, ::-1])
@@ -164,20 +174,26 @@ def test_n4096_gauss(r):
     first_interval_matches_oracle(4096, r, "gauss", "etb", 8)
     full_solve_properties(4096, r, "gauss", [
         {"strategy": "sync", "depth": 1}, {"strategy": "etb", "depth": 2},
-        {"strategy": "etb", "depth": 4}, {"strategy": "etb", "depth": 8}])
+        {"strategy": "etb", "depth": 4}, {"strategy": "etb", "depth": 8},
+        {"strategy": "sync", "depth": 1, "control": "device"},
+        {"strategy": "etb", "depth": 4, "control": "device"},
+        {"strategy": "etb", "depth": 8, "control": "device"}])
 
 
 def test_n8192_r100_gauss():
     first_interval_matches_oracle(8192, 100.0, "gauss", "etb", 4)
     full_solve_properties(8192, 100.0, "gauss", [
         {"strategy": "sync", "depth": 1}, {"strategy": "etb", "depth": 4},
-        {"strategy": "etb", "depth": 8}])
+        {"strategy": "etb", "depth": 8},
+        {"strategy": "etb", "depth": 4, "control": "device"}])
     full_solve_properties(8192, 100.0, "gauss", [
         {"strategy": "sync", "depth": 1, "check_every": 16},
-        {"strategy": "etb", "depth": 16}])
+        {"strategy": "etb", "depth": 16},
+        {"strategy": "etb", "depth": 16, "control": "device"}])
 
 
 def test_n18432_r10_point():
     first_interval_matches_oracle(18432, 10.0, "point", "etb", 8)
     full_solve_properties(18432, 10.0, "point", [
-        {"strategy": "sync", "depth": 1}, {"strategy": "etb", "depth": 8}])
+        {"strategy": "sync", "depth": 1}, {"strategy": "etb", "depth": 8},
+        {"strategy": "etb", "depth": 8, "control": "device"}])
