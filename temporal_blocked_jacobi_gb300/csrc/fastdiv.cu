@@ -1,6 +1,6 @@
-// Exhaustive verification of the fixed-divisor division (div_fixed in
-// jacobi_kernels.cuh) against the IEEE quotient, and the exact host-side
-// reciprocal it needs.
+// Exhaustive verification of the fixed-divisor division (div_fixed and its
+// packed form div2_fixed in jacobi_kernels.cuh) against the IEEE quotient,
+// and the exact host-side reciprocal it needs.
 #include <cmath>
 #include <cstring>
 
@@ -26,6 +26,12 @@ k_fastdiv_verify(float d, float y, unsigned long long *count) {
         const float want = __fdiv_rn(x, d);
         const float got = div_fixed(x, d, y);
         bad += (__float_as_uint(want) != __float_as_uint(got)) ? 1u : 0u;
+        // The packed form, on x and -x.
+        const float2 got2 = div2_fixed(make_float2(x, -x), make_float2(d, d),
+                                       make_float2(y, y));
+        bad += (__float_as_uint(want) != __float_as_uint(got2.x)) ? 1u : 0u;
+        bad += (__float_as_uint(__fdiv_rn(-x, d)) != __float_as_uint(got2.y))
+                   ? 1u : 0u;
     }
     for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
     if ((threadIdx.x & 31) == 0 && bad) atomicAdd(count, (unsigned long long)bad);

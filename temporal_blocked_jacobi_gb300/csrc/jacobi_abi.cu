@@ -402,7 +402,7 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
             (rc = make_map(h, &h->map_b, h->b)))
             return rc;
         TBJ_CUDA(h, c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED
-                        ? prepare_sweep_etb(h->tc)
+                        ? prepare_sweep_etb(h->tc, h->g.n)
                         : prepare_sweep_ba(h->tc));
     }
     h->per_launch = c.strategy == JACOBI_SYNC ? 1 : c.depth;

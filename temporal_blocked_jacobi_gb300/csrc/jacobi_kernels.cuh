@@ -32,6 +32,15 @@ __device__ __forceinline__ float div_fixed(float x, float d, float y) {
     return __fmaf_rn(-rho, y, q0);
 }
 
+// The same three steps on two numerators at once, with the packed float32
+// instructions of sm_100-class GPUs (per component numerically identical to
+// the scalar round-to-nearest operations).
+__device__ __forceinline__ float2 div2_fixed(float2 x, float2 d2, float2 y2) {
+    const float2 q0 = __fmul2_rn(x, y2);
+    const float2 rho = __ffma2_rn(q0, d2, make_float2(-x.x, -x.y));
+    return __ffma2_rn(make_float2(-rho.x, -rho.y), y2, q0);
+}
+
 template <bool FAST>
 __device__ __forceinline__ float div_d(float x, float d, float y) {
     if (FAST) return div_fixed(x, d, y);
@@ -294,6 +303,7 @@ struct TileConf {
     int threads;  // block size
     size_t smem;  // dynamic shared memory bytes
     int variant;  // compiled shape (exact temporal blocking)
+    int ctas;     // persistent grid size (exact temporal blocking)
 };
 
 // Exact temporal blocking (section 02 "Exact temporal blocking", after Meng
@@ -301,7 +311,8 @@ struct TileConf {
 int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc);
 // Raise the kernel's dynamic shared memory limit; call before any launch or
 // graph capture that uses `tc`.
-cudaError_t prepare_sweep_etb(const TileConf &tc);
+// (also sizes the persistent grid, tc.ctas)
+cudaError_t prepare_sweep_etb(TileConf &tc, int n);
 cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              const CUtensorMap *map_src,
                              const CUtensorMap *map_b, float *out,

@@ -11,15 +11,24 @@
 // boundary), the top/bottom halo D rows, so the tile is
 // TX = BX - 2*HX by TY = BY - 2*D cells.
 //
-// Thread 0 loads the box of u and the box of b with two TMA copies onto one
-// mbarrier (bounded wait). Each warp keeps its band's b in registers; the
-// field ping-pongs between two shared buffers. Sweep s updates rows
-// [s+1, BY-1-s) over the full box width: each lane streams down its band
-// holding rows i-1, i, i+1 in registers, with west/east neighbours from the
-// adjacent lanes by shuffle. Values near the box edge become inexact, but
-// inexactness moves inward one cell per sweep, so after D sweeps the tile
-// (HX >= D columns and D rows in from the edge) holds exactly the result of
-// D synchronous sweeps. The last sweep writes the tile to global memory.
+// The block is persistent: it walks tiles k, k + gridDim.x, ... Thread 0
+// loads a tile's box of u and of b with two TMA copies onto an mbarrier
+// (bounded wait); with NB = 2 buffer sets the next tile is loaded while the
+// current one is swept, with NB = 1 right after it. Each warp keeps its
+// band's b in registers; the field ping-pongs between two shared buffers,
+// each with a spare row above and below the box so that every row of every
+// band can be updated without a bounds test. In sweep s each warp updates
+// its whole band over the full box width -- bands lying entirely outside the
+// rows still needed, [s+1, BY-1-s), are skipped -- streaming down the band
+// with rows i-1, i, i+1 in registers and west/east neighbours from the
+// adjacent lanes by shuffle. Cells near the box edge (and the spare rows)
+// become inexact, but inexactness moves inward one cell per sweep, so after
+// D sweeps the tile (HX >= D columns and D rows in from the edge) holds
+// exactly the result of D synchronous sweeps. The last sweep writes the tile
+// to global memory.
+//
+// With the verified fixed-divisor division the update of a lane's four
+// cells uses packed float32 pairs for everything but the west+east sums.
 //
 // Dirichlet ring cells are never updated: in tiles whose box reaches past
 // the interior, a cell keeps its value unless it is an interior grid cell.
@@ -52,11 +61,16 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for phase 0 of the barrier, giving up after ~1 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar) {
-    if (mbar_try_wait(bar, 0)) return true;
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Wait for the given phase parity of a barrier, giving up after ~1 s.
+__device__ __forceinline__ bool mbar_wait_parity(uint64_t *bar, unsigned par) {
+    if (mbar_try_wait(bar, par)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, 0)) {
+    while (!mbar_try_wait(bar, par)) {
         if (global_ns() - t0 > 1000000000ull) return false;
     }
     return true;
@@ -72,15 +86,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
         : "memory");
 }
 
-template <int D, int CH, int RW, int NW>
+template <int D, int CH, int RW, int NW, int NB = 2>
 struct EtbShape {
     static constexpr int BX = 128 * CH;
     static constexpr int BY = NW * RW;
     static constexpr int HX = (D + 3) / 4 * 4;
     static constexpr int TX = BX - 2 * HX;
     static constexpr int TY = BY - 2 * D;
-    static constexpr size_t BUF = (size_t)BX * BY * sizeof(float);
-    static constexpr size_t SMEM = 256 + 2 * BUF;
+    // One buffer: the box plus a spare row above and below it. NB sets of
+    // two buffers (NB = 2: the current tile and the prefetched next one).
+    static constexpr size_t BUF = (size_t)BX * (BY + 2) * sizeof(float);
+    static constexpr size_t BOX_BYTES = (size_t)BX * BY * sizeof(float);
+    static constexpr size_t SMEM = 256 + 2 * NB * BUF;
     static_assert(TX >= 4 && TY >= 1, "tile too small for this depth");
     static_assert(BX <= 256 && BY <= 256, "TMA box dimension limit");
 };
@@ -92,15 +109,37 @@ __device__ __forceinline__ void sts4(float *p, float4 v) {
     *reinterpret_cast<float4 *>(p) = v;
 }
 
+// J for the four cells of a float4 chunk: n4, c4, s4 the rows above, at and
+// below, w/e the cells west of .x and east of .w.
 template <bool FAST>
 __device__ __forceinline__ float4 update4(float4 n4, float4 c4, float4 s4,
                                           float4 b4, float w, float e, float r,
                                           float d, float y) {
+    if (FAST) {
+        // Same operations, same order, mostly two cells per instruction:
+        // ((W+E) + (N+S)) * r + b, then the fixed-divisor division. The
+        // product r * s is formed with scalar round-to-nearest multiplies:
+        // a packed multiply feeding a packed add can be fused into one
+        // multiply-add by the compiler, which would change the rounding.
+        const float2 d2 = make_float2(d, d), y2 = make_float2(y, y);
+        const float2 h01 = make_float2(__fadd_rn(w, c4.y), __fadd_rn(c4.x, c4.z));
+        const float2 h23 = make_float2(__fadd_rn(c4.y, c4.w), __fadd_rn(c4.z, e));
+        const float2 v01 = __fadd2_rn(make_float2(n4.x, n4.y), make_float2(s4.x, s4.y));
+        const float2 v23 = __fadd2_rn(make_float2(n4.z, n4.w), make_float2(s4.z, s4.w));
+        const float2 s01 = __fadd2_rn(h01, v01), s23 = __fadd2_rn(h23, v23);
+        const float2 rs01 = make_float2(__fmul_rn(r, s01.x), __fmul_rn(r, s01.y));
+        const float2 rs23 = make_float2(__fmul_rn(r, s23.x), __fmul_rn(r, s23.y));
+        const float2 num01 = __fadd2_rn(make_float2(b4.x, b4.y), rs01);
+        const float2 num23 = __fadd2_rn(make_float2(b4.z, b4.w), rs23);
+        const float2 q01 = div2_fixed(num01, d2, y2);
+        const float2 q23 = div2_fixed(num23, d2, y2);
+        return make_float4(q01.x, q01.y, q23.x, q23.y);
+    }
     float4 o;
-    o.x = jacobi_update<FAST>(w, c4.y, n4.x, s4.x, b4.x, r, d, y);
-    o.y = jacobi_update<FAST>(c4.x, c4.z, n4.y, s4.y, b4.y, r, d, y);
-    o.z = jacobi_update<FAST>(c4.y, c4.w, n4.z, s4.z, b4.z, r, d, y);
-    o.w = jacobi_update<FAST>(c4.z, e, n4.w, s4.w, b4.w, r, d, y);
+    o.x = jacobi_update<false>(w, c4.y, n4.x, s4.x, b4.x, r, d, y);
+    o.y = jacobi_update<false>(c4.x, c4.z, n4.y, s4.y, b4.y, r, d, y);
+    o.z = jacobi_update<false>(c4.y, c4.w, n4.z, s4.z, b4.z, r, d, y);
+    o.w = jacobi_update<false>(c4.z, e, n4.w, s4.w, b4.w, r, d, y);
     return o;
 }
 
@@ -115,8 +154,10 @@ __device__ __forceinline__ float4 hold4(float4 nv, float4 old, bool row_ok,
     return o;
 }
 
+// D sweeps of one tile. sA, sB point at box row 0 of the two buffers (rows
+// -1 and BY exist); b of this warp's band is in breg.
 template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool FUSED>
-__device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
+__device__ __forceinline__ void etb_sweeps(float *sA, float *sB,
                                            const float4 (&breg)[RW][CH],
                                            float *__restrict__ out, int n,
                                            long long ld, float r, float d,
@@ -126,13 +167,15 @@ __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int band = warp * RW;
+    const int col = 4 * lane;  // this lane's column within a 128-wide chunk
+    const int left = (lane + 31) & 31, right = (lane + 1) & 31;
 
     // Columns of this lane's chunks that are interior grid cells (edge tiles).
     unsigned colmask[CH];
     bool in_tile[CH];
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
-        const int bx = 128 * c + 4 * lane;
+        const int bx = 128 * c + col;
         unsigned m = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -146,46 +189,46 @@ __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
 #pragma unroll 1
     for (int s = 0; s < D; ++s) {
         const float *src = (s & 1) ? sB : sA;
-        float *dst = (s & 1) ? const_cast<float *>(sA) : sB;
+        float *dst = (s & 1) ? sA : sB;
         const bool last = (s == D - 1);
-        const int rlo = max(s + 1, band);
-        const int rhi = min(S::BY - 1 - s, band + RW);
-        if (rlo < rhi) {
+        // Skip the band if none of its rows is still needed.
+        if (band + RW > s + 1 && band < S::BY - 1 - s) {
+            const float *sp = src + band * S::BX + col;
+            float *dp = dst + band * S::BX + col;
             float4 nr[CH], cr[CH];
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
-                nr[c] = lds4(src + (rlo - 1) * S::BX + 128 * c + 4 * lane);
-                cr[c] = lds4(src + rlo * S::BX + 128 * c + 4 * lane);
+                nr[c] = lds4(sp - S::BX + 128 * c);
+                cr[c] = lds4(sp + 128 * c);
             }
 #pragma unroll
             for (int j = 0; j < RW; ++j) {
-                const int row = band + j;
-                if (row < rlo || row >= rhi) continue;  // uniform per warp
                 float4 sr[CH];
 #pragma unroll
                 for (int c = 0; c < CH; ++c)
-                    sr[c] = lds4(src + (row + 1) * S::BX + 128 * c + 4 * lane);
+                    sr[c] = lds4(sp + (j + 1) * S::BX + 128 * c);
                 float wv[CH], ev[CH];
 #pragma unroll
                 for (int c = 0; c < CH; ++c) {
-                    wv[c] = __shfl_sync(FULL, cr[c].w, (lane + 31) & 31);
-                    ev[c] = __shfl_sync(FULL, cr[c].x, (lane + 1) & 31);
+                    wv[c] = __shfl_sync(FULL, cr[c].w, left);
+                    ev[c] = __shfl_sync(FULL, cr[c].x, right);
                 }
+                const int row = band + j;
                 const int gy = byo + row;
                 const bool row_ok = !EDGE || (gy >= 1 && gy <= n - 2);
+                const bool tile_row = row >= D && row < D + S::TY;
 #pragma unroll
                 for (int c = 0; c < CH; ++c) {
                     const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
                     const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
                     float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w,
                                               e, r, d, y);
-                    if (FUSED && s == 0 && in_tile[c] && row >= D &&
-                        row < D + S::TY && row_ok) {
+                    if (FUSED && s == 0 && in_tile[c] && tile_row && row_ok) {
                         // Residual of the launch's input at the tile's cells.
                         const float4 c4 = cr[c], n4 = nr[c], s4 = sr[c];
                         const float4 b4 = breg[j][c];
                         if (EDGE) {
-                            const int gx = bxo + 128 * c + 4 * lane;
+                            const int gx = bxo + 128 * c + col;
                             if (colmask[c] & 1u) cell_residual(nv.x, c4.x, w, c4.y, n4.x, s4.x, b4.x, gy, gx + 0, n, r, d, rm, bm);
                             if (colmask[c] & 2u) cell_residual(nv.y, c4.y, c4.x, c4.z, n4.y, s4.y, b4.y, gy, gx + 1, n, r, d, rm, bm);
                             if (colmask[c] & 4u) cell_residual(nv.z, c4.z, c4.y, c4.w, n4.z, s4.z, b4.z, gy, gx + 2, n, r, d, rm, bm);
@@ -204,9 +247,9 @@ __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
                     }
                     if (EDGE) nv = hold4(nv, cr[c], row_ok, colmask[c]);
                     if (!last) {
-                        sts4(dst + row * S::BX + 128 * c + 4 * lane, nv);
-                    } else if (in_tile[c] && row_ok) {
-                        float *g = out + (long long)gy * ld + (bxo + 128 * c + 4 * lane);
+                        sts4(dp + j * S::BX + 128 * c, nv);
+                    } else if (in_tile[c] && tile_row && row_ok) {
+                        float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
                         if (colmask[c] == 0xfu) {
                             sts4(g, nv);
                         } else {
@@ -225,96 +268,153 @@ __device__ __forceinline__ void etb_sweeps(const float *sA, float *sB,
     }
 }
 
-template <int D, int CH, int RW, int NW, bool FAST, bool FUSED>
-__global__ void __launch_bounds__(32 * NW)
+// Issue the TMA loads of one tile's box of u (into a) and of b (into bb).
+template <class S>
+__device__ __forceinline__ void load_tile(const CUtensorMap *map_src,
+                                          const CUtensorMap *map_b,
+                                          uint64_t *bar, float *a, float *bb,
+                                          int tile, int tiles_x, int depth) {
+    const int gx0 = (tile % tiles_x) * S::TX, gy0 = (tile / tiles_x) * S::TY;
+    asm volatile(
+        "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "r"((unsigned)(2 * S::BOX_BYTES))
+        : "memory");
+    tma_load_2d(a, map_src, bar, gx0 - S::HX, gy0 - depth);
+    tma_load_2d(bb, map_b, bar, gx0 - S::HX, gy0 - depth);
+}
+
+// Persistent kernel: block k handles tiles k, k + gridDim.x, ... (row-major
+// over a tiles_x-wide tile grid). With NB = 2 the TMA engine fills the other
+// buffer set with the next tile while the block sweeps the current one; with
+// NB = 1 the next tile's load is issued as soon as the current tile is done.
+template <int D, int CH, int RW, int NW, int NB, bool FAST, bool FUSED>
+__global__ void __launch_bounds__(32 * NW, 1)
 k_etb(const __grid_constant__ CUtensorMap map_src,
       const __grid_constant__ CUtensorMap map_b, float *__restrict__ out,
       int n, long long ld, float r, float d, float y, unsigned *err,
-      const int *stop, LoopParams lp) {
-    using S = EtbShape<D, CH, RW, NW>;
+      const int *stop, LoopParams lp, int tiles_x, int tiles) {
+    using S = EtbShape<D, CH, RW, NW, NB>;
+    static_assert(S::SMEM <= 227 * 1024, "shared memory per block");
     if (stop && *stop) return;  // same value for every thread of the launch
     __shared__ unsigned fin_scratch[65];
-    const int gx0 = blockIdx.x * S::TX;  // tile's first cell (grid coords)
-    const int gy0 = blockIdx.y * S::TY;
-    if (gx0 > n - 2 || gy0 > n - 2) {  // tile holds no interior cell
-        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
-        return;
-    }
-    const int bxo = gx0 - S::HX;  // grid coords of box cell (0,0)
-    const int byo = gy0 - D;
 
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(base);
-    float *sA = reinterpret_cast<float *>(base + 128);
-    float *sB = reinterpret_cast<float *>(base + 128 + S::BUF);
+    // Offsets from the __shared__ array itself, so that every access stays
+    // in the shared address space: [2 barriers | A0 | B0 | A1 | B1] (NB = 2),
+    // each buffer = spare row, BY box rows, spare row; rows are 512 or 1024
+    // bytes, so every box row is 128-byte aligned.
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + pad);
+    float *buf0 = reinterpret_cast<float *>(smem_raw + pad + 128);
+    constexpr int bufn = S::BX * (S::BY + 2);
 
     const int tid = threadIdx.x;
+    for (int k = tid; k < S::BX; k += 32 * NW)
+        for (int q = 0; q < 2 * NB; ++q) {
+            buf0[q * bufn + k] = 0.f;  // spare rows: finite values
+            buf0[q * bufn + (S::BY + 1) * S::BX + k] = 0.f;
+        }
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar))
-                     : "memory");
+        mbar_init(&bars[0]);
+        mbar_init(&bars[1]);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile(
-            "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                smem_addr(bar)),
-            "r"((unsigned)(2 * S::BUF))
-            : "memory");
-        tma_load_2d(sA, &map_src, bar, bxo, byo);
-        tma_load_2d(sB, &map_b, bar, bxo, byo);  // b staged in the B buffer
+        if ((int)blockIdx.x < tiles)
+            load_tile<S>(&map_src, &map_b, &bars[0], buf0 + S::BX,
+                         buf0 + bufn + S::BX, blockIdx.x, tiles_x, D);
     }
-    __syncthreads();
-    const bool ok = mbar_wait_bounded(bar);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) atomicOr(err, (unsigned)ERR_TMA_TIMEOUT);
-        mbar_wait_bounded(bar);
-        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
-        return;
-    }
-    // b of this warp's band into registers; then the B buffer is free.
-    const int lane = tid & 31;
-    const int band = (tid >> 5) * RW;
-    float4 breg[RW][CH];
-#pragma unroll
-    for (int j = 0; j < RW; ++j)
-#pragma unroll
-        for (int c = 0; c < CH; ++c)
-            breg[j][c] = lds4(sB + (band + j) * S::BX + 128 * c + 4 * lane);
     __syncthreads();
 
+    const int lane = tid & 31;
+    const int band = (tid >> 5) * RW;
     unsigned rm = 0u, bm = 0u;
-    const bool edge = bxo < 1 || byo < 1 || bxo + S::BX > n - 1 ||
-                      byo + S::BY > n - 1;
-    if (edge)
-        etb_sweeps<D, CH, RW, NW, FAST, true, FUSED>(sA, sB, breg, out, n, ld, r,
-                                                     d, y, bxo, byo, rm, bm);
-    else
-        etb_sweeps<D, CH, RW, NW, FAST, false, FUSED>(sA, sB, breg, out, n, ld,
-                                                      r, d, y, bxo, byo, rm, bm);
+    bool failed = false;
+    int fail_p = 0;
+    unsigned fail_parity = 0u;
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+        const int p = NB == 2 ? (i & 1) : 0;
+        float *sA = buf0 + (2 * p) * bufn + S::BX;  // box row 0
+        float *sB = buf0 + (2 * p + 1) * bufn + S::BX;
+        const unsigned parity = NB == 2 ? (unsigned)(i >> 1) & 1u : (unsigned)i & 1u;
+        const bool ok = mbar_wait_parity(&bars[p], parity);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            fail_p = p;
+            fail_parity = parity;
+            break;
+        }
+        float4 breg[RW][CH];
+#pragma unroll
+        for (int j = 0; j < RW; ++j)
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                breg[j][c] = lds4(sB + (band + j) * S::BX + 128 * c + 4 * lane);
+        // Everyone is past the previous tile (which used the other set) and
+        // holds this tile's b: prefetch the next tile into the other set.
+        __syncthreads();
+        if (NB == 2 && tid == 0 && t + (int)gridDim.x < tiles) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            load_tile<S>(&map_src, &map_b, &bars[p ^ 1],
+                         buf0 + (2 * (p ^ 1)) * bufn + S::BX,
+                         buf0 + (2 * (p ^ 1) + 1) * bufn + S::BX,
+                         t + gridDim.x, tiles_x, D);
+        }
+        const int gx0 = (t % tiles_x) * S::TX, gy0 = (t / tiles_x) * S::TY;
+        const int bxo = gx0 - S::HX, byo = gy0 - D;
+        const bool edge = bxo < 1 || byo < 1 || bxo + S::BX > n - 1 ||
+                          byo + S::BY > n - 1;
+        if (edge)
+            etb_sweeps<D, CH, RW, NW, FAST, true, FUSED>(sA, sB, breg, out, n, ld,
+                                                         r, d, y, bxo, byo, rm, bm);
+        else
+            etb_sweeps<D, CH, RW, NW, FAST, false, FUSED>(sA, sB, breg, out, n,
+                                                          ld, r, d, y, bxo, byo, rm,
+                                                          bm);
+        if (NB == 1 && t + (int)gridDim.x < tiles) {
+            __syncthreads();  // everyone is done with the single buffer set
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                load_tile<S>(&map_src, &map_b, &bars[0], buf0 + S::BX,
+                             buf0 + bufn + S::BX, t + gridDim.x, tiles_x, D);
+            }
+        }
+    }
+    if (failed) {
+        if (tid == 0) atomicOr(err, (unsigned)ERR_TMA_TIMEOUT);
+        // Only the load waited on can be in flight (the next one is issued
+        // after it lands): give it one more bounded wait before shared memory
+        // is released.
+        mbar_wait_parity(&bars[fail_p], fail_parity);
+    }
     if (FUSED) fused_block_finish(rm, bm, lp, fin_scratch);
 }
 
-// Shapes per depth: {CH, RW, NW}. Index 0 is the default.
+// Shapes per depth: {CH, RW, NW, NB}. The first one of a depth is its
+// default (fastest measured on GB300).
 struct EtbVariant {
-    int depth, ch, rw, nw;
+    int depth, ch, rw, nw, nb;
 };
 constexpr EtbVariant kVariants[] = {
-    {2, 1, 4, 16}, {2, 2, 4, 16},
-    {4, 1, 4, 16}, {4, 2, 4, 16},
-    {8, 1, 8, 16}, {8, 2, 4, 16},
-    {16, 2, 4, 24}, {16, 1, 6, 32},
+    {2, 1, 3, 32, 2}, {2, 1, 4, 16, 2}, {2, 2, 4, 16, 1},
+    {4, 1, 3, 32, 2}, {4, 1, 4, 16, 2}, {4, 2, 4, 16, 1},
+    {8, 1, 3, 32, 2}, {8, 1, 4, 16, 2}, {8, 1, 4, 32, 1}, {8, 2, 4, 16, 1},
+    {16, 1, 4, 32, 1}, {16, 1, 3, 32, 2}, {16, 2, 3, 32, 1},
 };
 
-template <int D, int CH, int RW, int NW>
-cudaError_t launch_variant(const GridDesc &g, const CUtensorMap *map_src,
+template <int D, int CH, int RW, int NW, int NB>
+cudaError_t launch_variant(const GridDesc &g, const TileConf &tc,
+                           const CUtensorMap *map_src,
                            const CUtensorMap *map_b, float *out,
                            unsigned *err, const LaunchCtl &ctl,
                            cudaStream_t stream) {
-    using S = EtbShape<D, CH, RW, NW>;
-    const dim3 grid((g.n + S::TX - 1) / S::TX, (g.n + S::TY - 1) / S::TY);
-#define TBJ_K(F, FU)                                                          \
-    k_etb<D, CH, RW, NW, F, FU><<<grid, 32 * NW, S::SMEM, stream>>>(          \
-        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, err, ctl.stop, ctl.lp)
+    using S = EtbShape<D, CH, RW, NW, NB>;
+    const int tiles_x = (g.n - 1 + S::TX - 1) / S::TX;
+    const int tiles = tiles_x * ((g.n - 1 + S::TY - 1) / S::TY);
+#define TBJ_K(F, FU)                                                            \
+    k_etb<D, CH, RW, NW, NB, F, FU><<<tc.ctas, 32 * NW, S::SMEM, stream>>>(     \
+        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, err, ctl.stop, ctl.lp, \
+        tiles_x, tiles)
     if (g.fast) {
         if (ctl.fused) TBJ_K(true, true);
         else TBJ_K(true, false);
@@ -326,37 +426,56 @@ cudaError_t launch_variant(const GridDesc &g, const CUtensorMap *map_src,
     return cudaGetLastError();
 }
 
-template <int D, int CH, int RW, int NW>
-cudaError_t prepare_variant() {
-    using S = EtbShape<D, CH, RW, NW>;
+template <int D, int CH, int RW, int NW, int NB>
+cudaError_t prepare_variant(TileConf &tc, int n) {
+    using S = EtbShape<D, CH, RW, NW, NB>;
     const void *kernels[4] = {
-        (const void *)k_etb<D, CH, RW, NW, true, false>,
-        (const void *)k_etb<D, CH, RW, NW, false, false>,
-        (const void *)k_etb<D, CH, RW, NW, true, true>,
-        (const void *)k_etb<D, CH, RW, NW, false, true>};
+        (const void *)k_etb<D, CH, RW, NW, NB, true, false>,
+        (const void *)k_etb<D, CH, RW, NW, NB, false, false>,
+        (const void *)k_etb<D, CH, RW, NW, NB, true, true>,
+        (const void *)k_etb<D, CH, RW, NW, NB, false, true>};
     for (const void *k : kernels) {
         cudaError_t e = cudaFuncSetAttribute(
             k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
         if (e != cudaSuccess) return e;
     }
+    // Persistent grid: as many blocks as fit on the GPU at once, at most one
+    // per tile.
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, k_etb<D, CH, RW, NW, NB, true, false>, 32 * NW, S::SMEM);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int tiles = ((n - 1 + S::TX - 1) / S::TX) * ((n - 1 + S::TY - 1) / S::TY);
+    tc.ctas = sms * per_sm < tiles ? sms * per_sm : tiles;
     return cudaSuccess;
 }
 
 // Dispatch on a variant index (into kVariants).
-#define TBJ_ETB_VARIANTS(X)          \
-    X(0, 2, 1, 4, 16)                \
-    X(1, 2, 2, 4, 16)                \
-    X(2, 4, 1, 4, 16)                \
-    X(3, 4, 2, 4, 16)                \
-    X(4, 8, 1, 8, 16)                \
-    X(5, 8, 2, 4, 16)                \
-    X(6, 16, 2, 4, 24)               \
-    X(7, 16, 1, 6, 32)
+#define TBJ_ETB_VARIANTS(X) \
+    X(0, 2, 1, 3, 32, 2)    \
+    X(1, 2, 1, 4, 16, 2)    \
+    X(2, 2, 2, 4, 16, 1)    \
+    X(3, 4, 1, 3, 32, 2)    \
+    X(4, 4, 1, 4, 16, 2)    \
+    X(5, 4, 2, 4, 16, 1)    \
+    X(6, 8, 1, 3, 32, 2)    \
+    X(7, 8, 1, 4, 16, 2)    \
+    X(8, 8, 1, 4, 32, 1)    \
+    X(9, 8, 2, 4, 16, 1)    \
+    X(10, 16, 1, 4, 32, 1)  \
+    X(11, 16, 1, 3, 32, 2)  \
+    X(12, 16, 2, 3, 32, 1)
 
 }  // namespace
 
 int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     (void)n;
+    if (depth != 2 && depth != 4 && depth != 8 && depth != 16) return -1;
     int pick = -1;
     for (int v = 0; v < (int)(sizeof(kVariants) / sizeof(kVariants[0])); ++v) {
         const EtbVariant &k = kVariants[v];
@@ -369,7 +488,6 @@ int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
             if (tile_x != 0 || tile_y != 0) break;
         }
     }
-    if (depth != 2 && depth != 4 && depth != 8 && depth != 16) return -1;
     if (pick < 0) return -5;
     const EtbVariant &k = kVariants[pick];
     tc->depth = depth;
@@ -381,16 +499,17 @@ int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->tile_y = tc->box_y - 2 * depth;
     tc->origin = 0;
     tc->threads = 32 * k.nw;
-    tc->smem = 256 + 2 * (size_t)tc->box_x * tc->box_y * sizeof(float);
+    tc->smem = 256 + 2 * (size_t)k.nb * tc->box_x * (tc->box_y + 2) * sizeof(float);
     tc->variant = pick;
+    tc->ctas = 0;  // set by prepare_sweep_etb
     return 0;
 }
 
-cudaError_t prepare_sweep_etb(const TileConf &tc) {
+cudaError_t prepare_sweep_etb(TileConf &tc, int n) {
     switch (tc.variant) {
-#define TBJ_PREP(I, D, CH, RW, NW) \
-    case I:                        \
-        return prepare_variant<D, CH, RW, NW>();
+#define TBJ_PREP(I, D, CH, RW, NW, NB) \
+    case I:                            \
+        return prepare_variant<D, CH, RW, NW, NB>(tc, n);
         TBJ_ETB_VARIANTS(TBJ_PREP)
 #undef TBJ_PREP
         default:
@@ -405,9 +524,9 @@ cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              cudaStream_t stream) {
     unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
     switch (tc.variant) {
-#define TBJ_LAUNCH(I, D, CH, RW, NW) \
-    case I:                          \
-        return launch_variant<D, CH, RW, NW>(g, map_src, map_b, out, err, ctl, stream);
+#define TBJ_LAUNCH(I, D, CH, RW, NW, NB) \
+    case I:                              \
+        return launch_variant<D, CH, RW, NW, NB>(g, tc, map_src, map_b, out, err, ctl, stream);
         TBJ_ETB_VARIANTS(TBJ_LAUNCH)
 #undef TBJ_LAUNCH
         default:

@@ -106,9 +106,11 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
     const int bxo = gx0 - hx;  // grid coordinates of box cell (0, 0)
     const int byo = gy0 - hy;
 
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *base = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    // Offsets from the __shared__ array itself keep every access in the
+    // shared address space.
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
+    unsigned char *base = smem_raw + pad;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base);
     const size_t buf = buffer_bytes(box_x, box_y);
     float *sA = reinterpret_cast<float *>(base + 128);
@@ -260,6 +262,7 @@ int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     const int cells = tile_x * tile_y;
     tc->threads = cells >= 512 ? 512 : (cells + 31) / 32 * 32;
     tc->variant = 0;
+    tc->ctas = 0;
     return finish_conf(tc);
 }
 
@@ -277,6 +280,7 @@ cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
 }
 
 int tiled_blocks(const GridDesc &g, const TileConf &tc) {
+    if (tc.ctas > 0) return tc.ctas;  // persistent grid
     return ((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x) *
            ((g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
 }

@@ -67,21 +67,23 @@ def test_rhs_sweep_residual_sync(n, pad, division):
         assert same_bits(np.float32(rm), rm_ref) and same_bits(np.float32(bm), bm_ref)
 
 
-# Compiled tile shapes of the exact-temporal-blocking kernel: (default, alternate).
-ETB_TILES = {2: [(0, 0), (248, 60)], 4: [(0, 0), (248, 56)],
-             8: [(0, 0), (240, 48)], 16: [(0, 0), (96, 160)]}
+# Compiled tile shapes of the exact-temporal-blocking kernel, per depth
+# ((0, 0) selects the default).
+ETB_TILES = {2: [(0, 0), (120, 60), (248, 60)],
+             4: [(0, 0), (120, 56), (248, 56)],
+             8: [(0, 0), (112, 48), (112, 112), (240, 48)],
+             16: [(0, 0), (96, 64), (224, 64)]}
+ETB_CASES = [(dd, t) for dd, ts in ETB_TILES.items() for t in ts]
 
 
 @pytest.mark.parametrize("n", [17, 70, 130, 259, 520, 1030])
-@pytest.mark.parametrize("depth", [2, 4, 8, 16])
-@pytest.mark.parametrize("alt", [0, 1])
+@pytest.mark.parametrize("depth,tile", ETB_CASES)
 @pytest.mark.parametrize("division", ["auto", "ieee"])
-def test_etb_launch_equals_depth_sync_sweeps(n, depth, alt, division):
+def test_etb_launch_equals_depth_sync_sweeps(n, depth, tile, division):
     """Exact temporal blocking: one launch = D synchronous sweeps, bit for
     bit (section 02, ghost-zone technique), for every compiled tile shape and
     both division paths."""
     r = 10.0 if depth != 16 else 100.0
-    tile = ETB_TILES[depth][alt]
     u0, g = fields(n, 8, seed=3 * n + depth)
     s, u, b = make_solver(u0, r, strategy="etb", depth=depth, tile=tile,
                           division=division)
