@@ -304,6 +304,9 @@ struct TileConf {
     size_t smem;  // dynamic shared memory bytes
     int variant;  // compiled shape (exact temporal blocking)
     int ctas;     // persistent grid size (exact temporal blocking)
+    // Block-asynchronous streaming kernel: super-tile sx x sy, ch float4
+    // chunks per lane, grid_x x grid_y blocks (stream = 0: generic kernel).
+    int stream, ch, sx, sy, grid_x, grid_y;
 };
 
 // Exact temporal blocking (section 02 "Exact temporal blocking", after Meng
@@ -330,5 +333,13 @@ cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             cudaStream_t stream);
 // Blocks of one launch of a tiled strategy (size of the fused partials).
 int tiled_blocks(const GridDesc &g, const TileConf &tc);
+// Streaming block-asynchronous kernel (kernels_ba.cu).
+bool ba_stream_configure(int n, TileConf *tc);
+cudaError_t prepare_sweep_ba_stream(const TileConf &tc);
+cudaError_t launch_sweep_ba_stream(const GridDesc &g, const TileConf &tc,
+                                   const CUtensorMap *map_src,
+                                   const CUtensorMap *map_b, float *out,
+                                   unsigned *err, const LaunchCtl &ctl,
+                                   cudaStream_t stream);
 
 }  // namespace tbj

@@ -502,6 +502,7 @@ int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->smem = 256 + 2 * (size_t)k.nb * tc->box_x * (tc->box_y + 2) * sizeof(float);
     tc->variant = pick;
     tc->ctas = 0;  // set by prepare_sweep_etb
+    tc->stream = tc->ch = tc->sx = tc->sy = tc->grid_x = tc->grid_y = 0;
     return 0;
 }
 

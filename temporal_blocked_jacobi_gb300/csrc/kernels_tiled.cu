@@ -263,10 +263,15 @@ int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->threads = cells >= 512 ? 512 : (cells + 31) / 32 * 32;
     tc->variant = 0;
     tc->ctas = 0;
+    tc->stream = tc->ch = tc->sx = tc->sy = tc->grid_x = tc->grid_y = 0;
+    // The streaming kernel takes every shape it can fit; the generic
+    // one-tile-per-block kernel below is kept for the rest.
+    if (ba_stream_configure(n, tc)) return 0;
     return finish_conf(tc);
 }
 
 cudaError_t prepare_sweep_ba(const TileConf &tc) {
+    if (tc.stream) return prepare_sweep_ba_stream(tc);
     return prepare_tiled(tc);
 }
 
@@ -276,11 +281,15 @@ cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             ResidualOut *status, const LaunchCtl &ctl,
                             cudaStream_t stream) {
     unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
+    if (tc.stream)
+        return launch_sweep_ba_stream(g, tc, map_src, map_b, out, err, ctl,
+                                      stream);
     return launch_tiled(g, tc, map_src, map_b, out, err, ctl, stream);
 }
 
 int tiled_blocks(const GridDesc &g, const TileConf &tc) {
     if (tc.ctas > 0) return tc.ctas;  // persistent grid
+    if (tc.stream) return tc.grid_x * tc.grid_y;
     return ((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x) *
            ((g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
 }
