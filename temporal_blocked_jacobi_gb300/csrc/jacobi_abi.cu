@@ -252,11 +252,20 @@ int record_batch(jacobi_handle_t *h, int start, cudaGraphExec_t *exec) {
     return JACOBI_OK;
 }
 
+// Check intervals per iteration of the device-side loop. Evaluating the
+// loop condition costs about as much as a launch, so an iteration runs about
+// eight launches' worth of intervals (launches after the stop return at
+// entry, so a few are wasted per time step). Even when an interval has an
+// odd number of launches, so that the body still ends in u.
+long long intervals_per_iteration(long long launches_per_check) {
+    const long long k = launches_per_check >= 8 ? 1 : 8 / launches_per_check;
+    return (launches_per_check % 2 == 1 && k % 2 == 1) ? k + 1 : k;
+}
+
 // Device control: record the graph of one time step,
 //   reset(LoopState) -> WHILE(cond) { body } -> copy LoopState to the host,
-// where the body is one check interval starting from u (fused first launch,
-// the rest honouring the stop flag); when an interval has an odd number of
-// launches the body holds two intervals so that it starts and ends in u.
+// where the body is intervals_per_iteration() check intervals starting from u,
+// each with a fused first launch and the rest honouring the stop flag.
 int record_step(jacobi_handle_t *h) {
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaGraphCreate(&graph, 0);
@@ -264,7 +273,7 @@ int record_step(jacobi_handle_t *h) {
     cudaGraphNode_t reset_node = nullptr, loop_node = nullptr;
     size_t count = 1;
     const long long L = h->launches_per_check;
-    const int halves = (L % 2 == 1) ? 2 : 1;
+    const long long halves = intervals_per_iteration(L);
     auto check = [&](cudaError_t err) {
         if (e == cudaSuccess) e = err;
         return e == cudaSuccess;
@@ -293,7 +302,7 @@ int record_step(jacobi_handle_t *h) {
         check(cudaStreamBeginCaptureToGraph(h->capture, body, nullptr, nullptr,
                                             0, cudaStreamCaptureModeThreadLocal))) {
         int src = 0;
-        for (int half = 0; half < halves; ++half)
+        for (long long half = 0; half < halves; ++half)
             for (long long l = 0; l < L; ++l) {
                 check(enqueue_launch(h, src, h->capture,
                                      loop_ctl(h, l == 0, src, cond)));
@@ -548,10 +557,10 @@ static long long solve_step_device(jacobi_handle_t *h) {
     TBJ_CUDA(h, cudaGraphLaunch(h->step, h->stream));
     TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
     const LoopState st = *h->loop_host;
-    // Launches run (no-ops after the stop included): one body per
-    // iteration; an iteration checks once (twice with two halves).
+    // Launches run (no-ops after the stop included): one body of
+    // intervals_per_iteration() intervals per iteration.
     const long long checks = st.result_k / h->interval + 1;
-    const long long per_body = h->launches_per_check % 2 == 1 ? 2 : 1;
+    const long long per_body = intervals_per_iteration(h->launches_per_check);
     const long long iters = (checks + per_body - 1) / per_body;
     h->launches += 1 + iters * per_body * h->launches_per_check;
     if (!st.stop)

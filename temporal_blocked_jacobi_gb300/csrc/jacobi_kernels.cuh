@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace tbj {
 
 // ---------------------------------------------------------------------------
@@ -269,6 +271,37 @@ __device__ __forceinline__ void cell_residual(float nv, float c, float w,
     const float bi = __fadd_rn(bb, __fmul_rn(r, q));
     rm = max(rm, abs_bits(res));
     bm = max(bm, abs_bits(bi));
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: a sweep kernel may be scheduled while the
+// previous kernel on its stream is still draining; it runs its set-up that
+// does not depend on that kernel (shared-memory carving, barrier init) and
+// then waits in grid_dependency_wait() until the previous grid has finished
+// and its writes are visible. It lets its own successor be scheduled early
+// with allow_dependents(). Both are no-ops for an ordinary launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Launch wrappers (all asynchronous on `stream`). They return the CUDA error

@@ -250,8 +250,8 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
      int sy, unsigned *err, const int *stop, LoopParams lp) {
     constexpr int BX = 128 * CH;
     constexpr int ROWS = kRowsMax + 2;
-    if (stop && *stop) return;  // same value for every thread of the launch
     __shared__ unsigned fin_scratch[65];
+    allow_dependents();
     const int bxo = blockIdx.x * sx;  // grid coords of box cell (0,0)
     const int byo = blockIdx.y * sy;
 
@@ -267,6 +267,11 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar))
                      : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // Everything below reads what the previous kernel wrote.
+    grid_dependency_wait();
+    if (stop && *stop) return;  // same value for every thread of the launch
+    if (tid == 0) {
         asm volatile(
             "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
                 smem_addr(bar)),
@@ -321,18 +326,12 @@ cudaError_t launch_ch(const GridDesc &g, const TileConf &tc,
     const dim3 grid(tc.grid_x, tc.grid_y), block(32 * NW);
     const size_t smem = smem_bytes<CH>();
 #define TBJ_K(F, FU)                                                           \
-    k_ba<CH, RW, NW, F, FU><<<grid, block, smem, stream>>>(                    \
-        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.depth, tc.tile_x,  \
-        tc.tile_y, tc.sx, tc.sy, err, ctl.stop, ctl.lp)
-    if (g.fast) {
-        if (ctl.fused) TBJ_K(true, true);
-        else TBJ_K(true, false);
-    } else {
-        if (ctl.fused) TBJ_K(false, true);
-        else TBJ_K(false, false);
-    }
+    launch_pdl(k_ba<CH, RW, NW, F, FU>, grid, block, smem, stream, *map_src,   \
+               *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.depth, tc.tile_x,     \
+               tc.tile_y, tc.sx, tc.sy, err, ctl.stop, ctl.lp)
+    if (g.fast) return ctl.fused ? TBJ_K(true, true) : TBJ_K(true, false);
+    return ctl.fused ? TBJ_K(false, true) : TBJ_K(false, false);
 #undef TBJ_K
-    return cudaGetLastError();
 }
 
 template <int CH, int RW, int NW>

@@ -296,8 +296,8 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
       const int *stop, LoopParams lp, int tiles_x, int tiles) {
     using S = EtbShape<D, CH, RW, NW, NB>;
     static_assert(S::SMEM <= 227 * 1024, "shared memory per block");
-    if (stop && *stop) return;  // same value for every thread of the launch
     __shared__ unsigned fin_scratch[65];
+    allow_dependents();
 
     // Offsets from the __shared__ array itself, so that every access stays
     // in the shared address space: [2 barriers | A0 | B0 | A1 | B1] (NB = 2),
@@ -319,10 +319,13 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
         mbar_init(&bars[0]);
         mbar_init(&bars[1]);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if ((int)blockIdx.x < tiles)
-            load_tile<S>(&map_src, &map_b, &bars[0], buf0 + S::BX,
-                         buf0 + bufn + S::BX, blockIdx.x, tiles_x, D);
     }
+    // Everything below reads what the previous kernel wrote.
+    grid_dependency_wait();
+    if (stop && *stop) return;  // same value for every thread of the launch
+    if (tid == 0 && (int)blockIdx.x < tiles)
+        load_tile<S>(&map_src, &map_b, &bars[0], buf0 + S::BX,
+                     buf0 + bufn + S::BX, blockIdx.x, tiles_x, D);
     __syncthreads();
 
     const int lane = tid & 31;
@@ -411,19 +414,13 @@ cudaError_t launch_variant(const GridDesc &g, const TileConf &tc,
     using S = EtbShape<D, CH, RW, NW, NB>;
     const int tiles_x = (g.n - 1 + S::TX - 1) / S::TX;
     const int tiles = tiles_x * ((g.n - 1 + S::TY - 1) / S::TY);
-#define TBJ_K(F, FU)                                                            \
-    k_etb<D, CH, RW, NW, NB, F, FU><<<tc.ctas, 32 * NW, S::SMEM, stream>>>(     \
-        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, err, ctl.stop, ctl.lp, \
-        tiles_x, tiles)
-    if (g.fast) {
-        if (ctl.fused) TBJ_K(true, true);
-        else TBJ_K(true, false);
-    } else {
-        if (ctl.fused) TBJ_K(false, true);
-        else TBJ_K(false, false);
-    }
+#define TBJ_K(F, FU)                                                           \
+    launch_pdl(k_etb<D, CH, RW, NW, NB, F, FU>, dim3(tc.ctas), dim3(32 * NW),  \
+               S::SMEM, stream, *map_src, *map_b, out, g.n, g.ld, g.r, g.d,   \
+               g.y, err, ctl.stop, ctl.lp, tiles_x, tiles)
+    if (g.fast) return ctl.fused ? TBJ_K(true, true) : TBJ_K(true, false);
+    return ctl.fused ? TBJ_K(false, true) : TBJ_K(false, false);
 #undef TBJ_K
-    return cudaGetLastError();
 }
 
 template <int D, int CH, int RW, int NW, int NB>

@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(32 * kWarps)
 k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
              float *__restrict__ out, int n, long long ld, float r, float d,
              float y, const int *stop, LoopParams lp) {
+    allow_dependents();
+    grid_dependency_wait();     // u, b and the stop flag come from before
     if (stop && *stop) return;  // same value for every thread of the launch
     const int lane = threadIdx.x;
     const int vx = blockIdx.x * 32 + lane;
@@ -346,19 +348,15 @@ cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
     const int rows = rows_per_warp(g.n);
     const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
 #define TBJ_SWEEP(R, F, FU)                                                   \
-    k_sweep_sync<R, F, FU><<<grid, block, 0, stream>>>(u, b, out, g.n, g.ld,  \
-                                                       g.r, g.d, g.y,         \
-                                                       ctl.stop, ctl.lp)
+    launch_pdl(k_sweep_sync<R, F, FU>, grid, block, 0, stream, u, b, out,     \
+               g.n, g.ld, g.r, g.d, g.y, ctl.stop, ctl.lp)
 #define TBJ_SWEEP_R(R)                                                        \
     case R:                                                                   \
-        if (g.fast) {                                                         \
-            if (ctl.fused) TBJ_SWEEP(R, true, true);                          \
-            else TBJ_SWEEP(R, true, false);                                   \
-        } else {                                                              \
-            if (ctl.fused) TBJ_SWEEP(R, false, true);                         \
-            else TBJ_SWEEP(R, false, false);                                  \
-        }                                                                     \
-        break;
+        if (g.fast)                                                           \
+            return ctl.fused ? TBJ_SWEEP(R, true, true)                       \
+                             : TBJ_SWEEP(R, true, false);                     \
+        return ctl.fused ? TBJ_SWEEP(R, false, true)                          \
+                         : TBJ_SWEEP(R, false, false);
     switch (rows) {
         TBJ_SWEEP_R(4)
         TBJ_SWEEP_R(8)
@@ -367,7 +365,7 @@ cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
     }
 #undef TBJ_SWEEP_R
 #undef TBJ_SWEEP
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 int sweep_sync_blocks(const GridDesc &g) {

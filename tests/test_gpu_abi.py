@@ -148,7 +148,9 @@ def test_device_control_launch_count(strategy, depth):
         per = 1 if strategy == "sync" else depth
         L = 8 // per if per <= 8 else 1
         checks = k // 8 + 1
-        body = 2 if L % 2 else 1
+        body = 1 if L >= 8 else 8 // L  # check intervals per loop iteration
+        if L % 2 and body % 2:
+            body += 1
         iters = -(-checks // body)
         copy = 1 if (L % 2 and checks % 2 == 0) else 0
         assert s.launch_count - c0 == 1 + iters * body * L + copy
