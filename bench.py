@@ -45,12 +45,15 @@ UNIT = "GLUP/s"
 WORKLOADS = {
     # name: (N, r, source, default strategies)
     "n512_r1_point": (512, 1.0, "point", "sync,etb2,etb4,etb8"),
-    "n2048_r10_gauss": (2048, 10.0, "gauss", "sync,etb2,etb4,etb8"),
-    "n8192_r100_gauss": (8192, 100.0, "gauss", "sync,etb4,etb8,etb16"),
+    "n2048_r10_gauss": (2048, 10.0, "gauss", "sync,syncu,etb2,etb4,etb8"),
+    "n8192_r100_gauss": (8192, 100.0, "gauss", "sync,syncu,etb4,etb8,etb16"),
     "n18432_r10_point": (18432, 10.0, "point", "sync,etb8,ba8"),
-    "n4096_r1_gauss": (4096, 1.0, "gauss", "sync,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16"),
-    "n4096_r10_gauss": (4096, 10.0, "gauss", "sync,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16"),
-    "n4096_r100_gauss": (4096, 100.0, "gauss", "sync,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16"),
+    "n4096_r1_gauss": (4096, 1.0, "gauss",
+                         "sync,syncu,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16,gasc8,gdesc8,gfb8"),
+    "n4096_r10_gauss": (4096, 10.0, "gauss",
+                         "sync,syncu,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16,gasc8,gdesc8,gfb8"),
+    "n4096_r100_gauss": (4096, 100.0, "gauss",
+                         "sync,syncu,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16,gasc8,gdesc8,gfb8"),
 }
 DEFAULT_WORKLOAD = "n2048_r10_gauss"
 TIME_STEPS = 10
@@ -58,7 +61,10 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
 def parse_strategy(tok: str):
-    """'sync' | 'etbD' | 'baD' | 'baD@TXxTY' -> kwargs for jacobi.Solver."""
+    """'sync' | 'syncu' | 'etbD' | 'baD' | 'gascD' | 'gdescD' | 'gfbD', each
+    optionally '@TXxTY' -> kwargs for jacobi.Solver. 'syncu': SYNC with the
+    unfused right-hand side; 'gasc', 'gdesc', 'gfb': BLOCK_ASYNC with that
+    depth controller and D up to the given depth (host control)."""
     tok = tok.strip()
     tile = (0, 0)
     if "@" in tok:
@@ -67,10 +73,22 @@ def parse_strategy(tok: str):
         tile = (int(tx), int(ty))
     if tok == "sync":
         return dict(strategy="sync", depth=1, tile=tile)
+    if tok == "syncu":
+        return dict(strategy="sync", depth=1, tile=tile, rhs="unfused")
+    for prefix, adapt in (("gasc", "g_asc"), ("gdesc", "g_desc"), ("gfb", "g_fb")):
+        if tok.startswith(prefix):
+            return dict(strategy="ba", depth=int(tok[len(prefix):]), tile=tile,
+                        adapt=adapt, control="host")
     for prefix, name in (("etb", "etb"), ("ba", "ba")):
         if tok.startswith(prefix):
             return dict(strategy=name, depth=int(tok[len(prefix):]), tile=tile)
     raise ValueError(f"unknown strategy {tok!r}")
+
+
+def bytes_per_point(kw):
+    """Algorithmic bytes per interior point per launch: read u, read b (u^n
+    and g when the right-hand side is unfused), write u'."""
+    return 16.0 if kw.get("rhs") == "unfused" else 12.0
 
 
 def sweeps_per_launch(kw):
@@ -211,9 +229,9 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for tok in strategies:
             kw = parse_strategy(tok)
+            kw.setdefault("control", args.control)
             u.copy_(u0)
-            solvers[tok] = jacobi.Solver(u, u_alt, b, r, stream=stream,
-                                         control=args.control, **kw)
+            solvers[tok] = jacobi.Solver(u, u_alt, b, r, stream=stream, **kw)
 
         def one_step(tok):
             """Reset u⁰ (setup, untimed) and run the ten time steps (timed)."""
@@ -252,8 +270,10 @@ def run_ours(args):
                     ms_per_solve_all=[round(t, 3) for t in times],
                     glups=interior * sweeps / (ms_med * 1e-3) / 1e9,
                     sync_equiv_gbs=12.0 * interior * sweeps / (ms_med * 1e-3) / 1e9,
-                    alg_gbs=12.0 * interior * sweeps / sweeps_per_launch(parse_strategy(tok))
-                    / (ms_med * 1e-3) / 1e9,
+                    # (D varies under a depth controller: not defined there)
+                    alg_gbs=None if parse_strategy(tok).get("adapt") else
+                    bytes_per_point(parse_strategy(tok)) * interior * sweeps
+                    / sweeps_per_launch(parse_strategy(tok)) / (ms_med * 1e-3) / 1e9,
                     launches=launches, total_ms=sum(times))
         torch.cuda.synchronize(dev)
         barrier()
@@ -268,6 +288,10 @@ def run_ours(args):
             res["sweep_ratio_s"] = res["sweeps"] / base["sweeps"]
             # cost per sweep relative to a synchronous sweep: S = 1/(c*s)
             res["cost_per_sweep_c"] = 1.0 / (res["speedup_vs_sync"] * res["sweep_ratio_s"])
+    if base and "syncu" in results:
+        # section 05, Table VI: T_unfused / T_fused of the synchronous sweep
+        results["syncu"]["t_unfused_over_fused"] = (
+            results["syncu"]["ms_per_solve_median"] / base["ms_per_solve_median"])
     total_ms = sum(res["total_ms"] for res in results.values())
     total_lups = sum(interior * res["sweeps"] * args.steps for res in results.values())
     lups_all, seconds_max = aggregate(float(interior * results[best]["sweeps"] * args.steps),
@@ -330,7 +354,7 @@ def kernel_roofline(solver, tok, u, u0, stream, interior, args):
     end.record(stream)
     end.synchronize()
     ms = start.elapsed_time(end) / launches
-    alg_bytes = 12.0 * interior  # read u, read b, write u' once per launch
+    alg_bytes = bytes_per_point(kw) * interior
     peak, how = measured_peaks()
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     traffic = load_traffic(tok, args.workload)
@@ -351,7 +375,7 @@ def kernel_roofline(solver, tok, u, u0, stream, interior, args):
 def kernel_name(tok):
     kw = parse_strategy(tok)
     if kw["strategy"] == "sync":
-        return "k_sweep_sync"
+        return "k_sweep_sync" + (" (unfused rhs)" if kw.get("rhs") == "unfused" else "")
     if kw["strategy"] == "etb":
         return f"k_etb (D={kw['depth']})"
     return f"k_ba / k_block_async (D={kw['depth']})"

@@ -84,6 +84,44 @@ typedef enum {
     JACOBI_DIVISION_IEEE = 1
 } jacobi_division_t;
 
+/* Where the right-hand side u^n + dt f is formed (section 02 and section 05,
+ * Table VI: the fused form is the fair synchronous baseline). Both give the
+ * same b_ij = fl(u^n_ij + g_ij) bit for bit, hence identical iterates. */
+typedef enum {
+    /* jacobi_rhs writes b = u^n + g once per time step; a sweep reads u and
+     * b: 12 bytes per cell. */
+    JACOBI_RHS_FUSED = 0,
+    /* jacobi_rhs keeps u^n in b and a copy of g in a buffer the handle
+     * allocates (N*ld floats); every sweep reads u, u^n and g and adds
+     * u^n + g itself: 16 bytes per cell. SYNC only. */
+    JACOBI_RHS_UNFUSED = 1
+} jacobi_rhs_t;
+
+/* Depth controllers for BLOCK_ASYNC (section 02: D is only a kernel
+ * argument, so it may change between launches). D changes only at a residual
+ * check, from the check's rho = rmax / bmax; the depths used are the powers
+ * of two 1, 2, 4, ... up to the config's `depth`. The controller starts
+ * afresh at every time step (jacobi_solve_step). */
+typedef enum {
+    JACOBI_ADAPT_NONE = 0,  /* fixed D = depth */
+    /* G-asc: D = 1 while rho >= 1e-2, then doubled each time rho first falls
+     * below 1e-2, 1e-3 and 1e-4; latched: a later rise of rho never lowers
+     * it again within the step. */
+    JACOBI_ADAPT_G_ASC = 1,
+    /* G-desc: the mirror image, D = depth halved at each of the same
+     * crossings (latched), never below 1. */
+    JACOBI_ADAPT_G_DESC = 2,
+    /* G-fb, hill climbing on the convergence rate per unit time: start at
+     * D = 1; at each check measure rate = -ln(rho_k / rho_{k-1}) / t_k, t_k
+     * the device time of the check interval in ms. The first measured rate
+     * doubles D; afterwards D doubles while the rate stays at or above 90%
+     * of the previously measured one and halves when it falls below (a drop
+     * of more than 10%); every measured rate becomes the next comparison
+     * point. After each change of D one measurement is skipped (settling:
+     * the residual bump the change causes). D stays within [1, depth]. */
+    JACOBI_ADAPT_G_FB = 3
+} jacobi_adapt_t;
+
 typedef struct {
     int strategy;         /* jacobi_strategy_t */
     int depth;            /* D: SYNC 1; EXACT_TEMPORAL_BLOCKED 2,4,8,16; BLOCK_ASYNC 1,2,4,8,16 */
@@ -95,7 +133,10 @@ typedef struct {
     long long max_sweeps; /* give up (JACOBI_ERR_NOT_CONVERGED) at this many sweeps; default 1<<22 */
     int control;          /* jacobi_control_t; default JACOBI_CONTROL_HOST */
     int division;         /* jacobi_division_t; default JACOBI_DIVISION_AUTO */
-    int reserved[2];      /* must be 0 */
+    int rhs;              /* jacobi_rhs_t; default JACOBI_RHS_FUSED */
+    int adapt;            /* jacobi_adapt_t; default JACOBI_ADAPT_NONE. Other
+                             values: BLOCK_ASYNC with depth 2, 4, 8 or 16 (the
+                             largest D) and JACOBI_CONTROL_HOST only */
 } jacobi_config_t;
 
 typedef struct jacobi_handle jacobi_handle_t;
@@ -123,10 +164,15 @@ int jacobi_create(jacobi_handle_t **out, int n, long long ld, float r,
                   float *b, void *cuda_stream);
 
 /*
- * Fused right-hand side (section 02: u^n + dt f is formed once per time
- * step instead of inside every sweep): b_ij = u_ij + g_ij on the interior,
- * one float32 add per cell. g is a device buffer in the grid layout (g = dt f).
- * Asynchronous on the handle's stream.
+ * Right-hand side of the next time step. With JACOBI_RHS_FUSED (section 02:
+ * u^n + dt f is formed once per time step instead of inside every sweep):
+ * b_ij = u_ij + g_ij on the interior, one float32 add per cell. With
+ * JACOBI_RHS_UNFUSED: b receives a copy of u (= u^n) and the handle's own
+ * buffer a copy of g, both on the interior; the sweeps form u^n + g. g is a
+ * device buffer in the grid layout (g = dt f); it may be freed or changed
+ * once this call's work has run. Asynchronous on the handle's stream. Call it
+ * again after changing the rhs mode with jacobi_set_strategy: a solve whose b
+ * was prepared for the other mode returns JACOBI_ERR_INVALID_ARG.
  */
 int jacobi_rhs(jacobi_handle_t *h, const float *g);
 
@@ -206,6 +252,55 @@ int jacobi_set_strategy(jacobi_handle_t *h, const jacobi_config_t *cfg);
  */
 long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
                      long long *sweeps_per_step);
+
+/*
+ * One residual check of the last jacobi_solve_step, in order. depth: D of the
+ * launches of that check interval; sweeps: sweeps done when the check was
+ * taken; rmax, bmax: its norms; ms: device time of the interval (its launches
+ * and the residual) from CUDA events, recorded under an adaptive depth
+ * controller only (0 otherwise).
+ */
+typedef struct {
+    int depth;
+    int pad;
+    long long sweeps;
+    float rmax, bmax;
+    float ms;
+    float pad2;
+} jacobi_check_record_t;
+
+/*
+ * Copy up to `cap` records of the last jacobi_solve_step's checks into rec
+ * (host memory; may be NULL when cap is 0). Returns the number of checks of
+ * that step (possibly more than cap) or a negative status. Recorded under
+ * JACOBI_CONTROL_HOST; under JACOBI_CONTROL_DEVICE the step's checks run on
+ * the device and 0 is returned.
+ */
+long long jacobi_check_trace(const jacobi_handle_t *h, jacobi_check_record_t *rec,
+                             long long cap);
+
+/*
+ * The depth controller alone (host code; no GPU needed), as an adaptive
+ * BLOCK_ASYNC solve runs it: jacobi_adapt_init starts it for one time step;
+ * after each check jacobi_adapt_next takes the check's rho = rmax / bmax and
+ * the interval's device time in ms and returns the D for the next interval
+ * (>= 1) or a negative status (bad state). The state is plain data.
+ */
+typedef struct {
+    int policy;        /* jacobi_adapt_t */
+    int depth;         /* D of the next interval */
+    int depth_max;     /* the config's depth */
+    int level;         /* G-asc / G-desc: thresholds crossed so far (latched) */
+    int settle;        /* G-fb: measurements still to skip */
+    int have_prev;     /* G-fb: rho_prev holds the previous check's rho */
+    int have_ref;      /* G-fb: rate_ref holds the previous measured rate */
+    int changes;       /* changes of D so far */
+    double rho_prev;
+    double rate_ref;
+} jacobi_adapt_state_t;
+
+int jacobi_adapt_init(jacobi_adapt_state_t *st, int policy, int depth_max);
+int jacobi_adapt_next(jacobi_adapt_state_t *st, double rho, double ms);
 
 /* Division the handle's kernels use: 1 = verified fixed-divisor division,
  * 0 = IEEE division, < 0 = error (NULL handle). */

@@ -11,6 +11,7 @@
 #include <map>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "../../include/jacobi.h"
 #include "jacobi_kernels.cuh"
@@ -21,6 +22,8 @@ struct jacobi_handle {
     GridDesc g;
     jacobi_config_t cfg;
     float *u = nullptr, *u_alt = nullptr, *b = nullptr;  // caller-owned
+    float *g_copy = nullptr;  // library-owned copy of g (unfused rhs only)
+    int b_mode = -1;          // rhs mode b was last prepared for (-1: none)
     cudaStream_t stream = nullptr;   // caller's stream: all work goes here
     cudaStream_t capture = nullptr;  // private stream used to record graphs
 
@@ -47,6 +50,16 @@ struct jacobi_handle {
     // Device control: one graph per time step (conditional WHILE loop).
     cudaGraphExec_t step = nullptr;
     int cur = 0;  // 0: the iterate is in u; 1: in u_alt
+
+    // Adaptive depth (BLOCK_ASYNC with a depth controller): one fixed-depth
+    // handle per D = 1, 2, 4, ... cfg.depth over the same buffers and stream,
+    // each with check graphs from both buffers.
+    jacobi_handle_t *level[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    int nlevels = 0;
+    cudaEvent_t ev[2] = {nullptr, nullptr};  // times each check interval
+
+    // Checks of the last solve_step (host control).
+    std::vector<jacobi_check_record_t> trace;
 
     long long launches = 0;  // kernels launched so far
     char err[512] = {0};
@@ -129,9 +142,25 @@ long long gcd_ll(long long a, long long b) {
 }
 
 int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
-    for (int k = 0; k < 2; ++k)
-        if (c.reserved[k])
-            return fail(h, JACOBI_ERR_INVALID_ARG, "reserved fields must be 0");
+    if (c.rhs != JACOBI_RHS_FUSED && c.rhs != JACOBI_RHS_UNFUSED)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "unknown rhs mode %d", c.rhs);
+    if (c.rhs == JACOBI_RHS_UNFUSED && c.strategy != JACOBI_SYNC)
+        return fail(h, JACOBI_ERR_UNSUPPORTED,
+                    "the unfused right-hand side is provided for SYNC only");
+    if (c.adapt < JACOBI_ADAPT_NONE || c.adapt > JACOBI_ADAPT_G_FB)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "unknown adapt %d", c.adapt);
+    if (c.adapt != JACOBI_ADAPT_NONE) {
+        if (c.strategy != JACOBI_BLOCK_ASYNC)
+            return fail(h, JACOBI_ERR_INVALID_ARG,
+                        "a depth controller needs BLOCK_ASYNC");
+        if (c.depth != 2 && c.depth != 4 && c.depth != 8 && c.depth != 16)
+            return fail(h, JACOBI_ERR_INVALID_ARG,
+                        "a depth controller takes depth 2, 4, 8 or 16 (the "
+                        "largest D)");
+        if (c.control != JACOBI_CONTROL_HOST)
+            return fail(h, JACOBI_ERR_UNSUPPORTED,
+                        "a depth controller runs under JACOBI_CONTROL_HOST");
+    }
     if (c.division != JACOBI_DIVISION_AUTO && c.division != JACOBI_DIVISION_IEEE)
         return fail(h, JACOBI_ERR_INVALID_ARG, "unknown division %d", c.division);
     if (c.check_every < 1)
@@ -212,6 +241,14 @@ cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
 cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
                            cudaStream_t s) {
     return enqueue_launch(h, src_is_alt, s, plain_ctl());
+}
+
+void destroy_levels(jacobi_handle_t *h) {
+    for (auto &l : h->level) {
+        if (l) jacobi_destroy(l);
+        l = nullptr;
+    }
+    h->nlevels = 0;
 }
 
 void destroy_graphs(jacobi_handle_t *h) {
@@ -380,8 +417,11 @@ int fast_division_ok(jacobi_handle_t *h, bool *ok) {
 }
 
 // Apply a (validated) configuration: tiles, tensor maps, graphs.
+int create_levels(jacobi_handle_t *h, const jacobi_config_t &c);
+
 int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     destroy_graphs(h);
+    destroy_levels(h);
     h->cfg = c;
     h->g.fast = false;
     if (c.division == JACOBI_DIVISION_AUTO) {
@@ -389,6 +429,18 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
         int rc = fast_division_ok(h, &ok);
         if (rc) return rc;
         h->g.fast = ok;
+    }
+    if (c.rhs == JACOBI_RHS_UNFUSED) {
+        if (!h->g_copy)
+        {
+            const size_t bytes = sizeof(float) * (size_t)h->g.n * (size_t)h->g.ld;
+            TBJ_CUDA(h, cudaMalloc(&h->g_copy, bytes));
+            // Ring and padding are read (never used) by the sweeps.
+            TBJ_CUDA(h, cudaMemsetAsync(h->g_copy, 0, bytes, h->stream));
+        }
+        h->g.g2 = h->g_copy;
+    } else {
+        h->g.g2 = nullptr;
     }
     int rc = 0;
     if (c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED)
@@ -428,6 +480,42 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     if ((rc = record_batch(h, 0, &h->batch[0]))) return rc;
     if (h->launches_per_check % 2 == 1)
         if ((rc = record_batch(h, 1, &h->batch[1]))) return rc;
+    if (c.adapt != JACOBI_ADAPT_NONE) return create_levels(h, c);
+    return JACOBI_OK;
+}
+
+// The fixed-depth handles an adaptive handle switches between. Each one's
+// check graphs exist for both start buffers, since the iterate may sit in
+// either when the controller picks its depth.
+int create_levels(jacobi_handle_t *h, const jacobi_config_t &c) {
+    jacobi_config_t lc = c;
+    lc.adapt = JACOBI_ADAPT_NONE;
+    lc.control = JACOBI_CONTROL_HOST;
+    int k = 0;
+    for (int d = 1; d <= c.depth; d *= 2, ++k) {
+        lc.depth = d;
+        jacobi_handle_t *l = nullptr;
+        int rc = jacobi_create(&l, h->g.n, h->g.ld, h->g.r, &lc, h->u,
+                               h->u_alt, h->b, h->stream);
+        if (rc) {
+            fail(h, rc, "creating the depth-%d solver: %s", d,
+                 jacobi_last_error(nullptr));
+            destroy_levels(h);
+            return rc;
+        }
+        h->level[k] = l;
+        h->nlevels = k + 1;
+        for (int start = 0; start < 2; ++start) {
+            if (l->batch[start]) continue;
+            if ((rc = record_batch(l, start, &l->batch[start]))) {
+                fail(h, rc, "depth-%d solver: %s", d, l->err);
+                destroy_levels(h);
+                return rc;
+            }
+        }
+    }
+    for (auto &e : h->ev)
+        if (!e) TBJ_CUDA(h, cudaEventCreate(&e));
     return JACOBI_OK;
 }
 
@@ -547,8 +635,24 @@ int jacobi_rhs(jacobi_handle_t *h, const float *g) {
         return fail(h, JACOBI_ERR_INVALID_ARG, "g must be a 16-byte aligned buffer");
     int rc = settle(h);
     if (rc) return rc;
-    TBJ_CUDA(h, launch_rhs(h->g, h->u, g, h->b, h->stream));
-    h->launches += 1;
+    if (h->cfg.rhs == JACOBI_RHS_UNFUSED) {
+        TBJ_CUDA(h, launch_copy_interior(h->g, h->u, h->b, h->stream));
+        TBJ_CUDA(h, launch_copy_interior(h->g, g, h->g_copy, h->stream));
+        h->launches += 2;
+    } else {
+        TBJ_CUDA(h, launch_rhs(h->g, h->u, g, h->b, h->stream));
+        h->launches += 1;
+    }
+    h->b_mode = h->cfg.rhs;
+    return JACOBI_OK;
+}
+
+// b must have been prepared by jacobi_rhs for the current rhs mode.
+static int check_b_mode(jacobi_handle_t *h) {
+    if (h->b_mode != -1 && h->b_mode != h->cfg.rhs)
+        return fail(h, JACOBI_ERR_INVALID_ARG,
+                    "the right-hand side was prepared for the other rhs mode; "
+                    "call jacobi_rhs again");
     return JACOBI_OK;
 }
 
@@ -589,8 +693,93 @@ static long long solve_step_device(jacobi_handle_t *h) {
     }
 }
 
+// Stopping rule at a check (section 01), shared by the host-driven loops:
+// 1 = stop (converged), 0 = continue, < 0 = a status to return.
+static int decide(jacobi_handle_t *h, const ResidualOut &ro, long long k) {
+    const double rm = (double)ro.rmax, bm = (double)ro.bmax;
+    if (!std::isfinite(rm) || !std::isfinite(bm))
+        return fail(h, JACOBI_ERR_NONFINITE,
+                    "residual norms not finite (rmax=%g, bmax=%g) after %lld "
+                    "sweeps",
+                    rm, bm, k);
+    if (rm == 0.0 || rm < h->cfg.tol * bm) return 1;
+    if (k >= h->cfg.max_sweeps)
+        return fail(h, JACOBI_ERR_NOT_CONVERGED,
+                    "not converged after %lld sweeps (rho=%g)", k,
+                    bm > 0 ? rm / bm : rm);
+    return 0;
+}
+
+static jacobi_check_record_t check_record(int depth, long long k,
+                                          const ResidualOut &ro, float ms) {
+    jacobi_check_record_t rec;
+    std::memset(&rec, 0, sizeof rec);
+    rec.depth = depth;
+    rec.sweeps = k;
+    rec.rmax = ro.rmax;
+    rec.bmax = ro.bmax;
+    rec.ms = ms;
+    return rec;
+}
+
+// One time step under a depth controller (section 02, G-asc / G-desc /
+// G-fb): each check interval runs the check graph of the fixed-depth handle
+// for the controller's current D, timed with CUDA events; the controller
+// then sees that check's rho and time.
+static long long solve_step_adaptive(jacobi_handle_t *h) {
+    jacobi_adapt_state_t st;
+    if (jacobi_adapt_init(&st, h->cfg.adapt, h->cfg.depth) != JACOBI_OK)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "bad depth controller");
+    long long k = 0;
+    int status = JACOBI_OK;
+    for (;;) {
+        int li = 0;
+        while ((1 << li) < st.depth) ++li;
+        if (li >= h->nlevels || !h->level[li])
+            return fail(h, JACOBI_ERR_INVALID_ARG, "no solver for depth %d",
+                        st.depth);
+        jacobi_handle_t *l = h->level[li];
+        TBJ_CUDA(h, cudaEventRecord(h->ev[0], h->stream));
+        TBJ_CUDA(h, cudaGraphLaunch(l->batch[h->cur], h->stream));
+        TBJ_CUDA(h, cudaEventRecord(h->ev[1], h->stream));
+        TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+        h->launches += l->launches_per_check + 1;
+        if (l->launches_per_check % 2 == 1) h->cur ^= 1;
+        k += l->interval;
+        float ms = 0.f;
+        TBJ_CUDA(h, cudaEventElapsedTime(&ms, h->ev[0], h->ev[1]));
+        const ResidualOut ro = *l->host_out;
+        h->trace.push_back(check_record(st.depth, k, ro, ms));
+        if (check_device_status(l, ro.err)) {
+            status = fail(h, JACOBI_ERR_CUDA, "%s", l->err);
+            break;
+        }
+        const int dec = decide(h, ro, k);
+        if (dec < 0) {
+            status = dec;
+            break;
+        }
+        if (dec == 1) break;
+        const double rm = (double)ro.rmax, bm = (double)ro.bmax;
+        const double rho = bm > 0.0 ? rm / bm : INFINITY;
+        if (jacobi_adapt_next(&st, rho, (double)ms) < 0)
+            return fail(h, JACOBI_ERR_INVALID_ARG, "depth controller failed");
+    }
+    int rc = settle(h);
+    if (rc) return rc;
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    return status ? status : k;
+}
+
 long long jacobi_solve_step(jacobi_handle_t *h) {
     if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (int rc = check_b_mode(h)) return rc;
+    h->trace.clear();
+    if (h->nlevels > 0) {
+        int rc = settle(h);
+        if (rc) return rc;
+        return solve_step_adaptive(h);
+    }
     if (h->cfg.control == JACOBI_CONTROL_DEVICE) {
         int rc = settle(h);
         if (rc) return rc;
@@ -606,22 +795,14 @@ long long jacobi_solve_step(jacobi_handle_t *h) {
         if (h->launches_per_check % 2 == 1) h->cur ^= 1;
         k += h->interval;
         const ResidualOut ro = *h->host_out;
+        h->trace.push_back(check_record(h->per_launch, k, ro, 0.f));
         if ((status = check_device_status(h, ro.err))) break;
-        const double rm = (double)ro.rmax, bm = (double)ro.bmax;
-        if (!std::isfinite(rm) || !std::isfinite(bm)) {
-            status = fail(h, JACOBI_ERR_NONFINITE,
-                          "residual norms not finite (rmax=%g, bmax=%g) after "
-                          "%lld sweeps",
-                          rm, bm, k);
+        const int dec = decide(h, ro, k);
+        if (dec < 0) {
+            status = dec;
             break;
         }
-        if (rm == 0.0 || rm < h->cfg.tol * bm) break;
-        if (k >= h->cfg.max_sweeps) {
-            status = fail(h, JACOBI_ERR_NOT_CONVERGED,
-                          "not converged after %lld sweeps (rho=%g)", k,
-                          bm > 0 ? rm / bm : rm);
-            break;
-        }
+        if (dec == 1) break;
     }
     int rc = settle(h);
     if (rc) return rc;
@@ -633,6 +814,7 @@ long long jacobi_sweeps(jacobi_handle_t *h, long long launches) {
     if (!h) return JACOBI_ERR_INVALID_ARG;
     if (launches < 0)
         return fail(h, JACOBI_ERR_INVALID_ARG, "launches must be >= 0");
+    if (int rc = check_b_mode(h)) return rc;
     for (long long l = 0; l < launches; ++l) {
         TBJ_CUDA(h, enqueue_launch(h, h->cur, h->stream));
         h->cur ^= 1;
@@ -647,6 +829,7 @@ int jacobi_residual(jacobi_handle_t *h, float *rmax, float *bmax) {
     if (!h) return JACOBI_ERR_INVALID_ARG;
     if (!rmax || !bmax)
         return fail(h, JACOBI_ERR_INVALID_ARG, "rmax and bmax must be non-NULL");
+    if (int rc0 = check_b_mode(h)) return rc0;
     int rc = settle(h);
     if (rc) return rc;
     TBJ_CUDA(h, launch_residual(h->g, h->u, h->b, h->partials, h->dev_out, 0,
@@ -695,16 +878,28 @@ long long jacobi_launch_count(const jacobi_handle_t *h) {
     return h ? h->launches : 0;
 }
 
+long long jacobi_check_trace(const jacobi_handle_t *h,
+                             jacobi_check_record_t *rec, long long cap) {
+    if (!h || cap < 0 || (cap > 0 && !rec)) return JACOBI_ERR_INVALID_ARG;
+    const long long n = (long long)h->trace.size();
+    for (long long i = 0; i < n && i < cap; ++i) rec[i] = h->trace[(size_t)i];
+    return n;
+}
+
 void jacobi_destroy(jacobi_handle_t *h) {
     if (!h) return;
     if (h->stream || h->capture) cudaStreamSynchronize(h->stream);
     destroy_graphs(h);
+    destroy_levels(h);
+    for (auto &e : h->ev)
+        if (e) cudaEventDestroy(e);
     if (h->capture) cudaStreamDestroy(h->capture);
     if (h->partials) cudaFree(h->partials);
     if (h->dev_out) cudaFree(h->dev_out);
     if (h->host_out) cudaFreeHost(h->host_out);
     if (h->loop) cudaFree(h->loop);
     if (h->loop_host) cudaFreeHost(h->loop_host);
+    if (h->g_copy) cudaFree(h->g_copy);
     delete h;
 }
 

@@ -89,6 +89,10 @@ struct GridDesc {
     float d;       // fl(1 + fl(4 r))
     float y;       // RN(1/d)
     bool fast;     // div_fixed verified equal to IEEE division for this d
+    // Unfused right-hand side (synchronous sweep only): when not null, the
+    // `b` argument of a launch holds u^n and every read of b_ij becomes
+    // fl(u^n_ij + g2_ij), the same value a fused b holds.
+    const float *g2 = nullptr;
 };
 
 // Result block of a residual reduction (device memory, one per handle).

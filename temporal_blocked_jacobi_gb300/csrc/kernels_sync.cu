@@ -56,8 +56,12 @@ struct RowIn {
     float edge;   // lane 0: u[i][x0-1]; lane 31: u[i][x0+4]; others unused
 };
 
+// UNF: b holds u^n and the right-hand side is formed here as fl(u^n + g)
+// (section 02: the unfused form reads both arrays on every sweep).
+template <bool UNF>
 __device__ __forceinline__ RowIn load_row(const float *__restrict__ u,
                                           const float *__restrict__ b,
+                                          const float *__restrict__ g,
                                           long long ld, int n, int i, int x0,
                                           int lane, bool active) {
     RowIn in;
@@ -68,6 +72,13 @@ __device__ __forceinline__ RowIn load_row(const float *__restrict__ u,
         const long long row = (long long)i * ld;
         in.bot = ld4(u + row + ld + x0);
         in.bb = ld4(b + row + x0);
+        if (UNF) {
+            const float4 gg = ld4(g + row + x0);
+            in.bb.x = __fadd_rn(in.bb.x, gg.x);
+            in.bb.y = __fadd_rn(in.bb.y, gg.y);
+            in.bb.z = __fadd_rn(in.bb.z, gg.z);
+            in.bb.w = __fadd_rn(in.bb.w, gg.w);
+        }
         if (lane == 0 && x0 > 0) in.edge = u[row + x0 - 1];
         if (lane == 31 && x0 + 4 < n) in.edge = u[row + x0 + 4];
     }
@@ -80,11 +91,12 @@ __device__ __forceinline__ RowIn load_row(const float *__restrict__ u,
 // residual norms of the input u (see LoopState); `stop`, when given, makes
 // the launch a no-op once the device-side loop has stopped.
 // ---------------------------------------------------------------------------
-template <int ROWS, bool FAST, bool FUSED>
+template <int ROWS, bool FAST, bool FUSED, bool UNF>
 __global__ void __launch_bounds__(32 * kWarps)
 k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
-             float *__restrict__ out, int n, long long ld, float r, float d,
-             float y, const int *stop, LoopParams lp) {
+             const float *__restrict__ g, float *__restrict__ out, int n,
+             long long ld, float r, float d, float y, const int *stop,
+             LoopParams lp) {
     allow_dependents();
     grid_dependency_wait();     // u, b and the stop flag come from before
     if (stop && *stop) return;  // same value for every thread of the launch
@@ -101,10 +113,11 @@ k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
             top = ld4(u + (long long)(i0 - 1) * ld + x0);
             mid = ld4(u + (long long)i0 * ld + x0);
         }
-        RowIn next = load_row(u, b, ld, n, i0, x0, lane, active);
+        RowIn next = load_row<UNF>(u, b, g, ld, n, i0, x0, lane, active);
         for (int i = i0; i < i1; ++i) {
             const RowIn cur = next;
-            if (i + 1 < i1) next = load_row(u, b, ld, n, i + 1, x0, lane, active);
+            if (i + 1 < i1)
+                next = load_row<UNF>(u, b, g, ld, n, i + 1, x0, lane, active);
             float west = __shfl_up_sync(FULL, mid.w, 1);
             float east = __shfl_down_sync(FULL, mid.x, 1);
             if (lane == 0) west = cur.edge;
@@ -178,11 +191,12 @@ __device__ __forceinline__ unsigned warp_max(unsigned v) {
     return v;
 }
 
-template <int ROWS, bool FAST>
+template <int ROWS, bool FAST, bool UNF>
 __global__ void __launch_bounds__(32 * kWarps)
-k_residual(const float *__restrict__ u, const float *__restrict__ b, int n,
-           long long ld, float r, float d, float y,
-           unsigned *__restrict__ partials, ResidualOut *__restrict__ out) {
+k_residual(const float *__restrict__ u, const float *__restrict__ b,
+           const float *__restrict__ g, int n, long long ld, float r, float d,
+           float y, unsigned *__restrict__ partials,
+           ResidualOut *__restrict__ out) {
     const int lane = threadIdx.x;
     const int vx = blockIdx.x * 32 + lane;
     const int x0 = vx * 4;
@@ -196,10 +210,11 @@ k_residual(const float *__restrict__ u, const float *__restrict__ b, int n,
             top = ld4(u + (long long)(i0 - 1) * ld + x0);
             mid = ld4(u + (long long)i0 * ld + x0);
         }
-        RowIn next = load_row(u, b, ld, n, i0, x0, lane, active);
+        RowIn next = load_row<UNF>(u, b, g, ld, n, i0, x0, lane, active);
         for (int i = i0; i < i1; ++i) {
             const RowIn cur = next;
-            if (i + 1 < i1) next = load_row(u, b, ld, n, i + 1, x0, lane, active);
+            if (i + 1 < i1)
+                next = load_row<UNF>(u, b, g, ld, n, i + 1, x0, lane, active);
             float west = __shfl_up_sync(FULL, mid.w, 1);
             float east = __shfl_down_sync(FULL, mid.x, 1);
             if (lane == 0) west = cur.edge;
@@ -347,16 +362,21 @@ cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
                               cudaStream_t stream) {
     const int rows = rows_per_warp(g.n);
     const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
-#define TBJ_SWEEP(R, F, FU)                                                   \
-    launch_pdl(k_sweep_sync<R, F, FU>, grid, block, 0, stream, u, b, out,     \
-               g.n, g.ld, g.r, g.d, g.y, ctl.stop, ctl.lp)
+#define TBJ_SWEEP(R, F, FU, UN)                                               \
+    launch_pdl(k_sweep_sync<R, F, FU, UN>, grid, block, 0, stream, u, b,      \
+               g.g2, out, g.n, g.ld, g.r, g.d, g.y, ctl.stop, ctl.lp)
+#define TBJ_SWEEP_F(R, F)                                                     \
+    if (g.g2)                                                                 \
+        return ctl.fused ? TBJ_SWEEP(R, F, true, true)                        \
+                         : TBJ_SWEEP(R, F, false, true);                      \
+    return ctl.fused ? TBJ_SWEEP(R, F, true, false)                           \
+                     : TBJ_SWEEP(R, F, false, false);
 #define TBJ_SWEEP_R(R)                                                        \
     case R:                                                                   \
-        if (g.fast)                                                           \
-            return ctl.fused ? TBJ_SWEEP(R, true, true)                       \
-                             : TBJ_SWEEP(R, true, false);                     \
-        return ctl.fused ? TBJ_SWEEP(R, false, true)                          \
-                         : TBJ_SWEEP(R, false, false);
+        if (g.fast) {                                                         \
+            TBJ_SWEEP_F(R, true)                                              \
+        }                                                                     \
+        TBJ_SWEEP_F(R, false)
     switch (rows) {
         TBJ_SWEEP_R(4)
         TBJ_SWEEP_R(8)
@@ -364,6 +384,7 @@ cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
         TBJ_SWEEP_R(32)
     }
 #undef TBJ_SWEEP_R
+#undef TBJ_SWEEP_F
 #undef TBJ_SWEEP
     return cudaErrorInvalidValue;
 }
@@ -390,14 +411,18 @@ cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
     const int rows = rows_per_warp(g.n);
     const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
     unsigned *part = reinterpret_cast<unsigned *>(partials);
+#define TBJ_RESID_K(R, F, UN)                                                 \
+    k_residual<R, F, UN><<<grid, block, 0, stream>>>(u, b, g.g2, g.n, g.ld,   \
+                                                     g.r, g.d, g.y, part, out)
 #define TBJ_RESID(R)                                                          \
     case R:                                                                   \
-        if (g.fast)                                                           \
-            k_residual<R, true><<<grid, block, 0, stream>>>(                  \
-                u, b, g.n, g.ld, g.r, g.d, g.y, part, out);                   \
-        else                                                                  \
-            k_residual<R, false><<<grid, block, 0, stream>>>(                 \
-                u, b, g.n, g.ld, g.r, g.d, g.y, part, out);                   \
+        if (g.fast) {                                                         \
+            if (g.g2) TBJ_RESID_K(R, true, true);                             \
+            else TBJ_RESID_K(R, true, false);                                 \
+        } else {                                                              \
+            if (g.g2) TBJ_RESID_K(R, false, true);                            \
+            else TBJ_RESID_K(R, false, false);                                \
+        }                                                                     \
         break;
     switch (rows) {
         TBJ_RESID(4)
@@ -406,6 +431,7 @@ cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
         TBJ_RESID(32)
     }
 #undef TBJ_RESID
+#undef TBJ_RESID_K
     return cudaGetLastError();
 }
 

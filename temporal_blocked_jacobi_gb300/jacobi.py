@@ -23,6 +23,11 @@ STRATEGIES = {"sync": SYNC, "etb": EXACT_TEMPORAL_BLOCKED,
 CONTROLS = {"host": CONTROL_HOST, "device": CONTROL_DEVICE}
 DIVISION_AUTO, DIVISION_IEEE = 0, 1
 DIVISIONS = {"auto": DIVISION_AUTO, "ieee": DIVISION_IEEE}
+RHS_FUSED, RHS_UNFUSED = 0, 1
+RHS_MODES = {"fused": RHS_FUSED, "unfused": RHS_UNFUSED}
+ADAPT_NONE, ADAPT_G_ASC, ADAPT_G_DESC, ADAPT_G_FB = 0, 1, 2, 3
+ADAPTS = {"none": ADAPT_NONE, "g_asc": ADAPT_G_ASC, "g_desc": ADAPT_G_DESC,
+          "g_fb": ADAPT_G_FB}
 
 
 class Config(ctypes.Structure):
@@ -30,7 +35,23 @@ class Config(ctypes.Structure):
                 ("tile_x", ctypes.c_int), ("tile_y", ctypes.c_int),
                 ("check_every", ctypes.c_int), ("tol", ctypes.c_double),
                 ("max_sweeps", ctypes.c_longlong), ("control", ctypes.c_int),
-                ("division", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+                ("division", ctypes.c_int), ("rhs", ctypes.c_int),
+                ("adapt", ctypes.c_int)]
+
+
+class CheckRecord(ctypes.Structure):
+    _fields_ = [("depth", ctypes.c_int), ("pad", ctypes.c_int),
+                ("sweeps", ctypes.c_longlong), ("rmax", ctypes.c_float),
+                ("bmax", ctypes.c_float), ("ms", ctypes.c_float),
+                ("pad2", ctypes.c_float)]
+
+
+class AdaptState(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int), ("depth", ctypes.c_int),
+                ("depth_max", ctypes.c_int), ("level", ctypes.c_int),
+                ("settle", ctypes.c_int), ("have_prev", ctypes.c_int),
+                ("have_ref", ctypes.c_int), ("changes", ctypes.c_int),
+                ("rho_prev", ctypes.c_double), ("rate_ref", ctypes.c_double)]
 
 
 class JacobiError(RuntimeError):
@@ -77,6 +98,10 @@ def load():
             "jacobi_last_error": (ctypes.c_char_p, [vp]),
             "jacobi_status_string": (ctypes.c_char_p, [i]),
             "jacobi_residual_noalloc": (i, [i, ll, f, vp, vp, vp, vp]),
+            "jacobi_check_trace": (ll, [vp, ctypes.POINTER(CheckRecord), ll]),
+            "jacobi_adapt_init": (i, [ctypes.POINTER(AdaptState), i, i]),
+            "jacobi_adapt_next": (i, [ctypes.POINTER(AdaptState), ctypes.c_double,
+                                      ctypes.c_double]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -112,9 +137,28 @@ def residual_noalloc(u, b, r, norms, stream=None) -> int:
         _ptr(norms), ctypes.c_void_p(stream.cuda_stream)))
 
 
+def adapt_depths(policy, depth_max, rhos, mss):
+    """Run the library's depth controller (jacobi_adapt_init / _next; host
+    code, no GPU) over one time step's checks: returns the D it picks after
+    each (rho, ms) pair, starting from [initial D]."""
+    st = AdaptState()
+    lib = load()
+    p = ADAPTS[policy] if isinstance(policy, str) else int(policy)
+    rc = lib.jacobi_adapt_init(ctypes.byref(st), p, int(depth_max))
+    if rc != OK:
+        raise JacobiError(rc, "jacobi_adapt_init")
+    out = [st.depth]
+    for rho, ms in zip(rhos, mss):
+        d = lib.jacobi_adapt_next(ctypes.byref(st), float(rho), float(ms))
+        if d < 0:
+            raise JacobiError(d, "jacobi_adapt_next")
+        out.append(int(d))
+    return out
+
+
 def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
                 tol=1e-5, max_sweeps=1 << 22, control="host",
-                division="auto") -> Config:
+                division="auto", rhs="fused", adapt="none") -> Config:
     c = Config()
     load().jacobi_config_default(ctypes.byref(c))
     c.strategy = STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
@@ -125,6 +169,8 @@ def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
     c.max_sweeps = int(max_sweeps)
     c.control = CONTROLS[control] if isinstance(control, str) else int(control)
     c.division = DIVISIONS[division] if isinstance(division, str) else int(division)
+    c.rhs = RHS_MODES[rhs] if isinstance(rhs, str) else int(rhs)
+    c.adapt = ADAPTS[adapt] if isinstance(adapt, str) else int(adapt)
     return c
 
 
@@ -158,7 +204,8 @@ class Solver:
 
     def __init__(self, u, u_alt, b, r, *, strategy="sync", depth=1,
                  tile=(0, 0), check_every=8, tol=1e-5, max_sweeps=1 << 22,
-                 control="host", division="auto", stream=None):
+                 control="host", division="auto", rhs="fused", adapt="none",
+                 stream=None):
         import torch
         lib = load()
         for t in (u, u_alt, b):
@@ -168,7 +215,7 @@ class Solver:
         self.stream = torch.cuda.current_stream(u.device) if stream is None else stream
         self._h = ctypes.c_void_p()
         cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
-                          control, division)
+                          control, division, rhs, adapt)
         with torch.cuda.device(u.device):
             rc = lib.jacobi_create(ctypes.byref(self._h), self.n, self.ld,
                                    float(r), ctypes.byref(cfg), _ptr(u),
@@ -213,9 +260,9 @@ class Solver:
 
     def set_strategy(self, strategy="sync", depth=1, tile=(0, 0),
                      check_every=8, tol=1e-5, max_sweeps=1 << 22, control="host",
-                     division="auto"):
+                     division="auto", rhs="fused", adapt="none"):
         cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
-                          control, division)
+                          control, division, rhs, adapt)
         self._ok(load().jacobi_set_strategy(self.handle, ctypes.byref(cfg)))
         self.config = cfg
 
@@ -227,6 +274,18 @@ class Solver:
         if total < 0:
             self._raise(total)
         return [int(counts[s]) for s in range(steps)]
+
+    def check_trace(self):
+        """The last solve_step's checks: list of dicts (depth, sweeps, rmax,
+        bmax, ms); empty under device control."""
+        lib = load()
+        n = lib.jacobi_check_trace(self.handle, None, 0)
+        if n < 0:
+            self._raise(n)
+        recs = (CheckRecord * max(int(n), 1))()
+        lib.jacobi_check_trace(self.handle, recs, int(n))
+        return [dict(depth=recs[i].depth, sweeps=recs[i].sweeps, rmax=recs[i].rmax,
+                     bmax=recs[i].bmax, ms=recs[i].ms) for i in range(int(n))]
 
     @property
     def division_mode(self) -> int:

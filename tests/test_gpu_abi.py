@@ -49,6 +49,35 @@ def test_invalid_arguments_rejected():
     assert e.value.status == jacobi.ERR_INVALID_ARG
 
 
+def test_rhs_mode_checked():
+    """The unfused right-hand side is SYNC-only; a solve whose b was prepared
+    for the other mode is refused until jacobi_rhs runs again."""
+    jacobi = _jacobi()
+    n = 40
+    u0, g = workload(n, "gauss")
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    with pytest.raises(jacobi.JacobiError) as e:
+        jacobi.Solver(u, u_alt, b, 1.0, strategy="etb", depth=4, rhs="unfused")
+    assert e.value.status == jacobi.ERR_UNSUPPORTED
+    with pytest.raises(jacobi.JacobiError) as e:
+        jacobi.Solver(u, u_alt, b, 1.0, rhs=7)
+    assert e.value.status == jacobi.ERR_INVALID_ARG
+    g_dev = to_dev(g)
+    with jacobi.Solver(u, u_alt, b, 1.0) as s:
+        s.rhs(g_dev)
+        s.set_strategy(rhs="unfused")
+        with pytest.raises(jacobi.JacobiError) as e:
+            s.solve_step()
+        assert e.value.status == jacobi.ERR_INVALID_ARG
+        s.rhs(g_dev)
+        k_unfused = s.solve_step()
+    u.copy_(to_dev(u0))
+    with jacobi.Solver(u, u_alt, b, 1.0) as s:
+        s.rhs(g_dev)
+        assert s.solve_step() == k_unfused
+
+
 def test_host_buffers_rejected():
     import ctypes
     jacobi = _jacobi()

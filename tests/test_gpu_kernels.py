@@ -67,6 +67,35 @@ def test_rhs_sweep_residual_sync(n, pad, division):
         assert same_bits(np.float32(rm), rm_ref) and same_bits(np.float32(bm), bm_ref)
 
 
+@pytest.mark.parametrize("n", [3, 5, 17, 70, 130, 259])
+@pytest.mark.parametrize("pad", [0, 12])
+@pytest.mark.parametrize("division", ["auto", "ieee"])
+def test_unfused_rhs_sweep_residual(n, pad, division):
+    """Unfused right-hand side (section 02; section 05, Table VI): b keeps
+    u^n and every sweep and residual forms fl(u^n + g) itself, the value the
+    fused b holds, so sweeps and norms match the oracle bit for bit."""
+    r = RS[(n + 1) % len(RS)]
+    u0, g = fields(n, pad, seed=7 * n + 1)
+    s, u, b = make_solver(u0, r, rhs="unfused", division=division)
+    with s:
+        s.rhs(to_dev(g))
+        assert same_bits(interior(b.cpu().numpy()), interior(u0))
+        b_ref = oracle.rhs(u0, g)
+        rm, bm = s.residual()
+        rm_ref, bm_ref = oracle.residual(u0, b_ref, r)
+        assert same_bits(np.float32(rm), rm_ref) and same_bits(np.float32(bm), bm_ref)
+        ref = u0
+        for launches in (1, 3):
+            s.sweeps(launches)
+            ref = oracle.sweeps(ref, b_ref, r, launches)
+            got = u.cpu().numpy()
+            assert same_bits(interior(got), interior(ref)), mismatch(got, ref)
+        assert np.isnan(got[:, n:]).all()
+        rm, bm = s.residual()
+        rm_ref, bm_ref = oracle.residual(ref, b_ref, r)
+        assert same_bits(np.float32(rm), rm_ref) and same_bits(np.float32(bm), bm_ref)
+
+
 # Compiled tile shapes of the exact-temporal-blocking kernel, per depth
 # ((0, 0) selects the default).
 ETB_TILES = {2: [(0, 0), (120, 60), (248, 60)],

@@ -52,6 +52,16 @@ def test_n2048_r10_gauss_bit_exact(n2048_reference, strategy, depth, control):
 
 
 @pytest.mark.parametrize("control", CONTROLS)
+def test_n2048_r10_gauss_unfused_sync_bit_exact(n2048_reference, control):
+    """The unfused right-hand side (section 05, Table VI) changes the
+    traffic, not the answer."""
+    u0, g, ref_u, ref_k = n2048_reference
+    got_u, got_k, _ = gpu_run(u0, g, 10.0, rhs="unfused", control=control)
+    assert got_k == ref_k
+    assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
+
+
+@pytest.mark.parametrize("control", CONTROLS)
 @pytest.mark.parametrize("n,r,source", [(130, 100.0, "gauss"), (70, 10.0, "point")])
 def test_etb16_checks_every_16_sweeps(n, r, source, control):
     """A 16-sweep launch is checked every lcm(8, 16) = 16 sweeps; it equals
@@ -177,7 +187,8 @@ def test_n4096_gauss(r):
         {"strategy": "etb", "depth": 4}, {"strategy": "etb", "depth": 8},
         {"strategy": "sync", "depth": 1, "control": "device"},
         {"strategy": "etb", "depth": 4, "control": "device"},
-        {"strategy": "etb", "depth": 8, "control": "device"}])
+        {"strategy": "etb", "depth": 8, "control": "device"},
+        {"strategy": "sync", "depth": 1, "rhs": "unfused", "control": "device"}])
 
 
 def test_n8192_r100_gauss():
