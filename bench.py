@@ -61,10 +61,12 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
 def parse_strategy(tok: str):
-    """'sync' | 'syncu' | 'etbD' | 'baD' | 'gascD' | 'gdescD' | 'gfbD', each
-    optionally '@TXxTY' -> kwargs for jacobi.Solver. 'syncu': SYNC with the
-    unfused right-hand side; 'gasc', 'gdesc', 'gfb': BLOCK_ASYNC with that
-    depth controller and D up to the given depth (host control)."""
+    """'sync' | 'syncu' | 'etbD' | 'baD' | 'baDoO' | 'gascD' | 'gdescD' |
+    'gfbD', each optionally '@TXxTY' -> kwargs for jacobi.Solver. 'syncu':
+    SYNC with the unfused right-hand side; 'baDoO': BLOCK_ASYNC on subdomains
+    overlapping by O cells in both directions; 'gasc', 'gdesc', 'gfb':
+    BLOCK_ASYNC with that depth controller and D up to the given depth (host
+    control)."""
     tok = tok.strip()
     tile = (0, 0)
     if "@" in tok:
@@ -79,6 +81,10 @@ def parse_strategy(tok: str):
         if tok.startswith(prefix):
             return dict(strategy="ba", depth=int(tok[len(prefix):]), tile=tile,
                         adapt=adapt, control="host")
+    if tok.startswith("ba") and "o" in tok:  # 'baDoO': overlap O both ways
+        depth, ov = tok[2:].split("o")
+        return dict(strategy="ba", depth=int(depth), tile=tile,
+                    overlap=(int(ov), int(ov)))
     for prefix, name in (("etb", "etb"), ("ba", "ba")):
         if tok.startswith(prefix):
             return dict(strategy=name, depth=int(tok[len(prefix):]), tile=tile)

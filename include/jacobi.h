@@ -124,7 +124,7 @@ typedef enum {
 
 typedef struct {
     int strategy;         /* jacobi_strategy_t */
-    int depth;            /* D: SYNC 1; EXACT_TEMPORAL_BLOCKED 2,4,8,16; BLOCK_ASYNC 1,2,4,8,16 */
+    int depth;            /* D: SYNC 1; EXACT_TEMPORAL_BLOCKED 2,4,8,16; BLOCK_ASYNC 1,2,4,8,16,32 */
     int tile_x, tile_y;   /* tile shape in cells; 0 = library default for the strategy.
                              tile_x a multiple of 4 for both tiled strategies;
                              BLOCK_ASYNC default 32 x 8 (section 02) */
@@ -137,6 +137,17 @@ typedef struct {
     int adapt;            /* jacobi_adapt_t; default JACOBI_ADAPT_NONE. Other
                              values: BLOCK_ASYNC with depth 2, 4, 8 or 16 (the
                              largest D) and JACOBI_CONTROL_HOST only */
+    int overlap_x, overlap_y; /* BLOCK_ASYNC overlapping subdomains ("Hierarchical
+                             Jacobi Iteration for Structured Matrices on GPUs
+                             using Shared Memory", overlapping subdomains in
+                             1-D and 2-D): tiles start every tile_x - overlap_x
+                             columns and tile_y - overlap_y rows, so
+                             neighbours share overlap_x columns (overlap_y
+                             rows); each tile sweeps all its cells against its
+                             frozen one-cell halo and writes back the cells
+                             of each shared band on its own side of the
+                             band's middle. Even, 0 <= overlap < tile size;
+                             default 0 (plain tiles). */
 } jacobi_config_t;
 
 typedef struct jacobi_handle jacobi_handle_t;

@@ -27,6 +27,14 @@ Functions and what pins them (tests/test_oracle_pins.py):
                                           sweeps; frozen-halo brute force on a
                                           2x2 tiling; mirror symmetry of a
                                           mirror-symmetric tiling
+  ba_overlap_launch  overlapping      -- pinned: overlap 0 equals ba_launch;
+                 subdomains ("Hierarchical Jacobi Iteration for Structured
+                 Matrices on GPUs using Shared Memory")
+                                          depth 1 equals one sweep; strips
+                                          brute-forced from synchronous sweeps
+                                          of each subdomain with its frozen
+                                          halo as the ring; mirror symmetry;
+                                          fewer sweeps with overlap
   run            ten-step driver       -- pinned through the above
 """
 from __future__ import annotations
@@ -85,13 +93,17 @@ def _load():
             f = getattr(lib, f"oracle_ba_launch_{sfx}")
             f.argtypes = [c_int, c_ll, real, c_int, c_int, c_int, rp, rp, rp]
             f.restype = c_int
+            f = getattr(lib, f"oracle_ba_overlap_launch_{sfx}")
+            f.argtypes = [c_int, c_ll, real, c_int, c_int, c_int, c_int, c_int,
+                          rp, rp, rp]
+            f.restype = c_int
             f = getattr(lib, f"oracle_solve_step_{sfx}")
             f.argtypes = [c_int, c_ll, real, c_int, c_d, c_ll, c_int, c_int,
-                          c_int, rp, rp, rp, preal, preal]
+                          c_int, c_int, c_int, rp, rp, rp, preal, preal]
             f.restype = c_ll
             f = getattr(lib, f"oracle_run_{sfx}")
             f.argtypes = [c_int, c_ll, real, c_int, c_d, c_ll, c_int, c_int,
-                          c_int, c_int, rp, rp, rp, rp, i64p]
+                          c_int, c_int, c_int, c_int, rp, rp, rp, rp, i64p]
             f.restype = c_ll
         _lib = lib
         return lib
@@ -167,11 +179,26 @@ def ba_launch(u, b, r, tile_x, tile_y, depth, n=None):
     return out
 
 
+def ba_overlap_launch(u, b, r, tile_x, tile_y, overlap_x, overlap_y, depth,
+                      n=None):
+    """One block-asynchronous launch on overlapping subdomains (tiles start
+    every tile - overlap cells; shared cells split half and half)."""
+    ld = _check(u, b)
+    n = u.shape[0] if n is None else n
+    out = u.copy()
+    rc = getattr(_load(), f"oracle_ba_overlap_launch_{_sfx(u)}")(
+        n, ld, _real(u)(r), tile_x, tile_y, overlap_x, overlap_y, depth, u, b, out)
+    if rc:
+        raise ValueError(f"oracle_ba_overlap_launch failed ({rc})")
+    return out
+
+
 def solve_step(u, b, r, *, m=8, tol=1e-5, max_sweeps=1 << 22, depth=0,
-               tile_x=32, tile_y=8, n=None):
+               tile_x=32, tile_y=8, overlap=(0, 0), n=None):
     """Solve one step in place from the warm start u. Returns
     (status_or_sweeps, rmax, bmax). depth 0 = synchronous sweeps; depth ≥ 1 =
-    block-asynchronous launches on tile_x×tile_y tiles."""
+    block-asynchronous launches on tile_x×tile_y tiles (overlapping by
+    `overlap` = (ox, oy) cells when not zero)."""
     ld = _check(u, b)
     n = u.shape[0] if n is None else n
     work = u.copy()
@@ -179,12 +206,12 @@ def solve_step(u, b, r, *, m=8, tol=1e-5, max_sweeps=1 << 22, depth=0,
     rm, bm = real(), real()
     k = getattr(_load(), f"oracle_solve_step_{_sfx(u)}")(
         n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
-        u, work, b, ctypes.byref(rm), ctypes.byref(bm))
+        overlap[0], overlap[1], u, work, b, ctypes.byref(rm), ctypes.byref(bm))
     return int(k), _real(u)(rm.value), _real(u)(bm.value)
 
 
 def run(u0, g, r, *, steps=10, m=8, tol=1e-5, max_sweeps=1 << 22, depth=0,
-        tile_x=32, tile_y=8, n=None):
+        tile_x=32, tile_y=8, overlap=(0, 0), n=None):
     """Run `steps` backward-Euler steps from u⁰. Returns (u_final, sweeps per
     step as a list, b of the last step). Raises on a negative status."""
     ld = _check(u0, g)
@@ -194,8 +221,8 @@ def run(u0, g, r, *, steps=10, m=8, tol=1e-5, max_sweeps=1 << 22, depth=0,
     b = np.zeros_like(u0)
     counts = np.zeros(steps, dtype=np.int64)
     rc = getattr(_load(), f"oracle_run_{_sfx(u)}")(
-        n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y, steps,
-        u, g, work, b, counts)
+        n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
+        overlap[0], overlap[1], steps, u, g, work, b, counts)
     if rc < 0:
         raise RuntimeError(f"oracle run failed with status {rc}: {counts.tolist()}")
     return u, counts.tolist(), b

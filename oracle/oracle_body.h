@@ -194,6 +194,81 @@ int FN(oracle_ba_launch)(int n, long long ld, REAL r, int tx, int ty,
     return 0;
 }
 
+/*
+ * Number of subdomains of t cells that start every t - o cells and together
+ * cover ni cells ("Hierarchical Jacobi Iteration for Structured Matrices on
+ * GPUs using Shared Memory", Eqs. 8-9: (N - o) / (tpb - o) blocks, rounded up
+ * so that the last one reaches the end; one subdomain when t >= ni).
+ */
+static int FN(subdomains)(int ni, int t, int o) {
+    if (ni <= t) return 1;
+    return (ni - o + (t - o) - 1) / (t - o);
+}
+
+/*
+ * One block-asynchronous launch on overlapping subdomains (same page, the
+ * sections on overlapping subdomains in 1-D and 2-D, Eqs. 15-16).
+ * Subdomain (p, q) holds the tx-by-ty interior cells starting at interior
+ * column p*(tx-ox) and row q*(ty-oy) (cut at the grid's edge), plus a
+ * one-cell halo. It is swept `depth` times against that halo frozen at its
+ * value at launch, exactly as in oracle_ba_launch. Two neighbouring
+ * subdomains share ox columns (oy rows); of these the left (upper) one
+ * contributes the left (upper) half to `out` and the right (lower) one the
+ * other half, the half that lies further from each one's edge. ox, oy even,
+ * 0 <= ox < tx, 0 <= oy < ty; with ox = oy = 0 this is oracle_ba_launch.
+ */
+int FN(oracle_ba_overlap_launch)(int n, long long ld, REAL r, int tx, int ty,
+                                 int ox, int oy, int depth, const REAL *u,
+                                 const REAL *b, REAL *out) {
+    if (tx < 1 || ty < 1 || depth < 1 || ox < 0 || oy < 0 || ox % 2 ||
+        oy % 2 || ox >= tx || oy >= ty)
+        return -1;
+    const int ni = n - 2;
+    const int kx = FN(subdomains)(ni, tx, ox), ky = FN(subdomains)(ni, ty, oy);
+    REAL d = FN(diag)(r);
+    int lw = tx + 2, lh = ty + 2;
+    REAL *cur = (REAL *)malloc(sizeof(REAL) * (size_t)lw * (size_t)lh);
+    REAL *nxt = (REAL *)malloc(sizeof(REAL) * (size_t)lw * (size_t)lh);
+    if (!cur || !nxt) { free(cur); free(nxt); return -2; }
+    for (int q = 0; q < ky; ++q) {
+        int y0 = 1 + q * (ty - oy);
+        int h = (y0 + ty <= n - 1) ? ty : (n - 1 - y0);
+        /* rows this subdomain writes: [wy0, wy1) */
+        int wy0 = y0 + (q > 0 ? oy / 2 : 0);
+        int wy1 = (q < ky - 1) ? y0 + ty - oy / 2 : y0 + h;
+        for (int p = 0; p < kx; ++p) {
+            int x0 = 1 + p * (tx - ox);
+            int w = (x0 + tx <= n - 1) ? tx : (n - 1 - x0);
+            int wx0 = x0 + (p > 0 ? ox / 2 : 0);
+            int wx1 = (p < kx - 1) ? x0 + tx - ox / 2 : x0 + w;
+            for (int a = 0; a < h + 2; ++a)
+                for (int c = 0; c < w + 2; ++c) {
+                    REAL v = u[(long long)(y0 - 1 + a) * ld + (x0 - 1 + c)];
+                    cur[a * lw + c] = v;
+                    nxt[a * lw + c] = v;
+                }
+            for (int sweep = 0; sweep < depth; ++sweep) {
+                for (int a = 1; a <= h; ++a)
+                    for (int c = 1; c <= w; ++c) {
+                        long long pp = (long long)(y0 - 1 + a) * ld + (x0 - 1 + c);
+                        nxt[a * lw + c] = FN(jacobi_point)(
+                            cur[a * lw + c - 1], cur[a * lw + c + 1],
+                            cur[(a - 1) * lw + c], cur[(a + 1) * lw + c],
+                            b[pp], r, d);
+                    }
+                REAL *t = cur; cur = nxt; nxt = t;
+            }
+            for (int gy = wy0; gy < wy1; ++gy)
+                for (int gx = wx0; gx < wx1; ++gx)
+                    out[(long long)gy * ld + gx] =
+                        cur[(gy - y0 + 1) * lw + (gx - x0 + 1)];
+        }
+    }
+    free(cur);
+    free(nxt);
+    return 0;
+}
+
 static long long FN(gcd)(long long a, long long b) {
     while (b) { long long t = a % b; a = b; b = t; }
     return a;
@@ -219,8 +294,8 @@ static long long FN(gcd)(long long a, long long b) {
  */
 long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
                                 double tol, long long max_sweeps, int depth,
-                                int tx, int ty, REAL *u, REAL *work,
-                                const REAL *b, REAL *rmax_out,
+                                int tx, int ty, int ox, int oy, REAL *u,
+                                REAL *work, const REAL *b, REAL *rmax_out,
                                 REAL *bmax_out) {
     if (n < 3 || ld < n || m < 1 || depth < 0) return -1;
     long long per_launch = depth == 0 ? 1 : depth;
@@ -234,7 +309,11 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
         for (long long l = 0; l < launches_per_check; ++l) {
             if (depth == 0)
                 FN(oracle_sweep)(n, ld, r, cur, b, nxt);
-            else if (FN(oracle_ba_launch)(n, ld, r, tx, ty, depth, cur, b, nxt))
+            else if (ox == 0 && oy == 0) {
+                if (FN(oracle_ba_launch)(n, ld, r, tx, ty, depth, cur, b, nxt))
+                    return -1;
+            } else if (FN(oracle_ba_overlap_launch)(n, ld, r, tx, ty, ox, oy,
+                                                    depth, cur, b, nxt))
                 return -1;
             REAL *t = cur; cur = nxt; nxt = t;
         }
@@ -260,12 +339,13 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
  */
 long long FN(oracle_run)(int n, long long ld, REAL r, int m, double tol,
                          long long max_sweeps, int depth, int tx, int ty,
-                         int steps, REAL *u, const REAL *g, REAL *work,
-                         REAL *b, long long *sweeps) {
+                         int ox, int oy, int steps, REAL *u, const REAL *g,
+                         REAL *work, REAL *b, long long *sweeps) {
     for (int s = 0; s < steps; ++s) {
         FN(oracle_rhs)(n, ld, u, g, b);
         long long k = FN(oracle_solve_step)(n, ld, r, m, tol, max_sweeps,
-                                            depth, tx, ty, u, work, b, 0, 0);
+                                            depth, tx, ty, ox, oy, u, work, b,
+                                            0, 0);
         sweeps[s] = k;
         if (k < 0) return k;
     }

@@ -183,9 +183,9 @@ int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
             break;
         case JACOBI_BLOCK_ASYNC:
             if (c.depth != 1 && c.depth != 2 && c.depth != 4 && c.depth != 8 &&
-                c.depth != 16)
+                c.depth != 16 && c.depth != 32)
                 return fail(h, JACOBI_ERR_INVALID_ARG,
-                            "BLOCK_ASYNC takes depth 1, 2, 4, 8 or 16");
+                            "BLOCK_ASYNC takes depth 1, 2, 4, 8, 16 or 32");
             break;
         default:
             return fail(h, JACOBI_ERR_INVALID_ARG, "unknown strategy %d",
@@ -193,6 +193,15 @@ int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     }
     if (c.tile_x < 0 || c.tile_y < 0)
         return fail(h, JACOBI_ERR_INVALID_ARG, "tile sizes must be >= 0");
+    if (c.overlap_x || c.overlap_y) {
+        if (c.strategy != JACOBI_BLOCK_ASYNC)
+            return fail(h, JACOBI_ERR_INVALID_ARG,
+                        "overlapping subdomains need BLOCK_ASYNC");
+        if (c.overlap_x < 0 || c.overlap_y < 0 || c.overlap_x % 2 ||
+            c.overlap_y % 2)
+            return fail(h, JACOBI_ERR_INVALID_ARG,
+                        "overlaps must be even and >= 0");
+    }
     return JACOBI_OK;
 }
 
@@ -446,12 +455,13 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     if (c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED)
         rc = etb_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc);
     else if (c.strategy == JACOBI_BLOCK_ASYNC)
-        rc = ba_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc);
+        rc = ba_configure(h->g.n, c.depth, c.tile_x, c.tile_y, c.overlap_x,
+                          c.overlap_y, &h->tc);
     if (rc == -1)
         return fail(h, JACOBI_ERR_INVALID_ARG,
-                    "tile %dx%d not valid for this strategy (tile_x must be a "
-                    "multiple of 4)",
-                    c.tile_x, c.tile_y);
+                    "tile %dx%d (overlap %dx%d) not valid for this strategy "
+                    "(tile_x a multiple of 4, overlaps smaller than the tile)",
+                    c.tile_x, c.tile_y, c.overlap_x, c.overlap_y);
     if (rc)
         return fail(h, JACOBI_ERR_UNSUPPORTED,
                     "tile %dx%d with depth %d needs a TMA box over 256 or more "

@@ -342,8 +342,11 @@ struct TileConf {
     int variant;  // compiled shape (exact temporal blocking)
     int ctas;     // persistent grid size (exact temporal blocking)
     // Block-asynchronous streaming kernel: super-tile sx x sy, ch float4
-    // chunks per lane, grid_x x grid_y blocks (stream = 0: generic kernel).
+    // chunks per lane, grid_x x grid_y blocks (stream = 0: generic kernel,
+    // one tile per block on a grid_x x grid_y grid).
     int stream, ch, sx, sy, grid_x, grid_y;
+    // Block-asynchronous overlapping subdomains (generic kernel only).
+    int overlap_x, overlap_y;
 };
 
 // Exact temporal blocking (section 02 "Exact temporal blocking", after Meng
@@ -361,7 +364,11 @@ cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
 
 // Block-asynchronous sweep (section 02 "Block-asynchronous"): one-cell
 // halo frozen at launch, all tile cells updated D times.
-int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc);
+// overlap_x, overlap_y: cells neighbouring tiles share (even, smaller than
+// the tile; "Hierarchical Jacobi Iteration for Structured Matrices on GPUs
+// using Shared Memory", overlapping subdomains); 0 = plain tiles.
+int ba_configure(int n, int depth, int tile_x, int tile_y, int overlap_x,
+                 int overlap_y, TileConf *tc);
 cudaError_t prepare_sweep_ba(const TileConf &tc);
 cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const CUtensorMap *map_src,

@@ -11,9 +11,19 @@
 // Cells on the Dirichlet ring and cells outside the grid (which the TMA load
 // fills with zeros) are never updated; no updated cell reads a cell outside
 // the grid. The box's left edge is kept on a 16-byte boundary (TMA rule):
-// tiles start at column 1 + k*TX with TX a multiple of 4, so the box starts
-// at k*TX and is TX + 4 columns wide; the extra columns are loaded and
-// ignored.
+// tile k starts at column 1 + k*SX, the box at (k*SX) rounded down to a
+// multiple of 4, and the box is TX + 4 columns wide; the extra columns are
+// loaded and ignored.
+//
+// Overlapping subdomains ("Hierarchical Jacobi Iteration for Structured
+// Matrices on GPUs using Shared Memory", overlapping subdomains in 1-D and
+// 2-D): with overlaps OX, OY (even, smaller than the tile) tiles start every
+// SX = TX - OX columns and SY = TY - OY rows, so neighbours share OX columns
+// (OY rows). Every tile sweeps all its cells, but writes back only the cells
+// it owns: of each shared band the nearer half, i.e. it leaves out OX/2
+// columns (OY/2 rows) next to each edge it shares with another tile. With
+// OX = OY = 0 this is the plain block-asynchronous launch; with OX even the rounding of the box start shifts the tile at
+// most 2 columns into the box, which TX + 4 columns still hold.
 #include <cudaTypedefs.h>
 
 #include "jacobi_kernels.cuh"
@@ -88,23 +98,39 @@ __host__ __device__ inline size_t buffer_bytes(int box_x, int box_y) {
     return round128((size_t)box_x * box_y * sizeof(float));
 }
 
+// Tile geometry of one launch (see the overlapping-subdomain note above).
+struct TileGeom {
+    int tx, ty;      // tile size
+    int sx, sy;      // distance between tile starts (tile - overlap)
+    int ox2, oy2;    // half overlaps: cells left to the neighbour per edge
+    int box_x, box_y;
+};
+
 template <int D, bool FAST, bool FUSED>
 __global__ void __launch_bounds__(512)
 k_block_async(const __grid_constant__ CUtensorMap map_src,
               const __grid_constant__ CUtensorMap map_b,
               float *__restrict__ out, int n, long long ld, float r, float d,
-              float y, int tx, int ty, int hx, int hy, int box_x, int box_y,
-              int origin, unsigned *err, const int *stop, LoopParams lp) {
+              float y, TileGeom tg, unsigned *err, const int *stop,
+              LoopParams lp) {
     if (stop && *stop) return;  // same value for every thread of the launch
     __shared__ unsigned fin_scratch[65];
-    const int gx0 = origin + blockIdx.x * tx;  // tile's first cell (grid)
-    const int gy0 = origin + blockIdx.y * ty;
-    if (gx0 > n - 2 || gy0 > n - 2 || gx0 + tx <= 1 || gy0 + ty <= 1) {
+    const int tx = tg.tx, ty = tg.ty, box_x = tg.box_x, box_y = tg.box_y;
+    const int gx0 = 1 + blockIdx.x * tg.sx;  // tile's first cell (grid)
+    const int gy0 = 1 + blockIdx.y * tg.sy;
+    if (gx0 > n - 2 || gy0 > n - 2) {
         if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
         return;
     }
-    const int bxo = gx0 - hx;  // grid coordinates of box cell (0, 0)
-    const int byo = gy0 - hy;
+    // Box origin: one cell up, and left to a 16-byte boundary.
+    const int bxo = (gx0 - 1) & ~3;
+    const int byo = gy0 - 1;
+    const int hx = gx0 - bxo, hy = 1;  // box position of the tile's first cell
+    // Cells this tile writes back (grid coordinates, half-open).
+    const int wx0 = gx0 + (blockIdx.x > 0 ? tg.ox2 : 0);
+    const int wx1 = gx0 + tx - (blockIdx.x + 1 < gridDim.x ? tg.ox2 : 0);
+    const int wy0 = gy0 + (blockIdx.y > 0 ? tg.oy2 : 0);
+    const int wy1 = gy0 + ty - (blockIdx.y + 1 < gridDim.y ? tg.oy2 : 0);
 
     // Offsets from the __shared__ array itself keep every access in the
     // shared address space.
@@ -154,17 +180,22 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
         for (int by = r0 + warp; by < r1; by += nwarps) {
             const float *row = src + by * box_x;
             const float *brow = sBb + by * box_x;
+            const int gy = byo + by;
+            const bool own_row = gy >= wy0 && gy < wy1;
             for (int bx = c0 + lane; bx < c1; bx += 32) {
                 const float w = row[bx - 1], e = row[bx + 1];
                 const float nn = row[bx - box_x], ss = row[bx + box_x];
                 const float v = jacobi_update<FAST>(w, e, nn, ss, brow[bx], r, d, y);
-                if (FUSED && s == 0)  // residual of the launch's input
-                    cell_residual(v, row[bx], w, e, nn, ss, brow[bx], byo + by,
-                                  bxo + bx, n, r, d, rm, bm);
-                if (last)
-                    out[(long long)(byo + by) * ld + (bxo + bx)] = v;
-                else
+                const int gx = bxo + bx;
+                const bool own = own_row && gx >= wx0 && gx < wx1;
+                if (FUSED && s == 0 && own)  // residual of the launch's input
+                    cell_residual(v, row[bx], w, e, nn, ss, brow[bx], gy, gx,
+                                  n, r, d, rm, bm);
+                if (last) {
+                    if (own) out[(long long)gy * ld + gx] = v;
+                } else {
                     dst[by * box_x + bx] = v;
+                }
             }
         }
         if (!last) __syncthreads();
@@ -176,14 +207,21 @@ cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
                          const CUtensorMap *map_src, const CUtensorMap *map_b,
                          float *out, unsigned *err, const LaunchCtl &ctl,
                          cudaStream_t stream) {
-    const dim3 grid((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x,
-                    (g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
+    const dim3 grid(tc.grid_x, tc.grid_y);
     const dim3 block(tc.threads);
+    TileGeom tg;
+    tg.tx = tc.tile_x;
+    tg.ty = tc.tile_y;
+    tg.sx = tc.tile_x - tc.overlap_x;
+    tg.sy = tc.tile_y - tc.overlap_y;
+    tg.ox2 = tc.overlap_x / 2;
+    tg.oy2 = tc.overlap_y / 2;
+    tg.box_x = tc.box_x;
+    tg.box_y = tc.box_y;
 #define TBJ_K(DD, F, FU)                                                      \
     k_block_async<DD, F, FU><<<grid, block, tc.smem, stream>>>(               \
-        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tc.tile_x,           \
-        tc.tile_y, tc.halo_x, tc.halo_y, tc.box_x, tc.box_y, tc.origin, err,  \
-        ctl.stop, ctl.lp)
+        *map_src, *map_b, out, g.n, g.ld, g.r, g.d, g.y, tg, err, ctl.stop,   \
+        ctl.lp)
 #define TBJ_LAUNCH(DD)                                                        \
     case DD:                                                                  \
         if (g.fast) {                                                         \
@@ -200,6 +238,7 @@ cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,
         TBJ_LAUNCH(4)
         TBJ_LAUNCH(8)
         TBJ_LAUNCH(16)
+        TBJ_LAUNCH(32)
         default:
             return cudaErrorInvalidValue;
     }
@@ -228,6 +267,7 @@ cudaError_t prepare_tiled(const TileConf &tc) {
         case 4: return prepare_depth<4>(tc.smem);
         case 8: return prepare_depth<8>(tc.smem);
         case 16: return prepare_depth<16>(tc.smem);
+        case 32: return prepare_depth<32>(tc.smem);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -243,18 +283,30 @@ int finish_conf(TileConf *tc) {
 
 }  // namespace
 
-int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
-    if (depth != 1 && depth != 2 && depth != 4 && depth != 8 && depth != 16)
+// Tiles of t cells starting every t - o cells needed to cover ni cells (at
+// least one).
+int subdomain_count(int ni, int t, int o) {
+    if (ni <= t) return 1;
+    return (ni - o + (t - o) - 1) / (t - o);
+}
+
+int ba_configure(int n, int depth, int tile_x, int tile_y, int overlap_x,
+                 int overlap_y, TileConf *tc) {
+    if (depth != 1 && depth != 2 && depth != 4 && depth != 8 && depth != 16 &&
+        depth != 32)
         return -1;
     if (tile_x == 0) tile_x = 32;
     if (tile_y == 0) tile_y = 8;
     if (tile_x < 4 || tile_x % 4 != 0 || tile_y < 1) return -1;
-    (void)n;
+    if (overlap_x < 0 || overlap_y < 0 || overlap_x % 2 || overlap_y % 2 ||
+        overlap_x >= tile_x || overlap_y >= tile_y)
+        return -1;
     tc->depth = depth;
     tc->tile_x = tile_x;
     tc->tile_y = tile_y;
-    tc->halo_x = 1;  // box starts one column left of the tile (aligned:
-                     // the tile starts at 1 + k * tile_x)
+    tc->overlap_x = overlap_x;
+    tc->overlap_y = overlap_y;
+    tc->halo_x = 1;  // box starts at most 3 columns left of the tile
     tc->halo_y = 1;
     tc->box_x = tile_x + 4;  // tile + 2 halo columns, rounded to 16 bytes
     tc->box_y = tile_y + 2;
@@ -263,10 +315,12 @@ int ba_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->threads = cells >= 512 ? 512 : (cells + 31) / 32 * 32;
     tc->variant = 0;
     tc->ctas = 0;
-    tc->stream = tc->ch = tc->sx = tc->sy = tc->grid_x = tc->grid_y = 0;
-    // The streaming kernel takes every shape it can fit; the generic
-    // one-tile-per-block kernel below is kept for the rest.
-    if (ba_stream_configure(n, tc)) return 0;
+    tc->stream = tc->ch = tc->sx = tc->sy = 0;
+    tc->grid_x = subdomain_count(n - 2, tile_x, overlap_x);
+    tc->grid_y = subdomain_count(n - 2, tile_y, overlap_y);
+    // The streaming kernel takes every non-overlapping shape it can fit; the
+    // generic one-tile-per-block kernel below is kept for the rest.
+    if (overlap_x == 0 && overlap_y == 0 && ba_stream_configure(n, tc)) return 0;
     return finish_conf(tc);
 }
 
@@ -288,10 +342,9 @@ cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
 }
 
 int tiled_blocks(const GridDesc &g, const TileConf &tc) {
+    (void)g;
     if (tc.ctas > 0) return tc.ctas;  // persistent grid
-    if (tc.stream) return tc.grid_x * tc.grid_y;
-    return ((g.n - tc.origin + tc.tile_x - 1) / tc.tile_x) *
-           ((g.n - tc.origin + tc.tile_y - 1) / tc.tile_y);
+    return tc.grid_x * tc.grid_y;
 }
 
 }  // namespace tbj

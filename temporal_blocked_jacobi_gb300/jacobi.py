@@ -36,7 +36,8 @@ class Config(ctypes.Structure):
                 ("check_every", ctypes.c_int), ("tol", ctypes.c_double),
                 ("max_sweeps", ctypes.c_longlong), ("control", ctypes.c_int),
                 ("division", ctypes.c_int), ("rhs", ctypes.c_int),
-                ("adapt", ctypes.c_int)]
+                ("adapt", ctypes.c_int), ("overlap_x", ctypes.c_int),
+                ("overlap_y", ctypes.c_int)]
 
 
 class CheckRecord(ctypes.Structure):
@@ -158,7 +159,8 @@ def adapt_depths(policy, depth_max, rhos, mss):
 
 def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
                 tol=1e-5, max_sweeps=1 << 22, control="host",
-                division="auto", rhs="fused", adapt="none") -> Config:
+                division="auto", rhs="fused", adapt="none",
+                overlap=(0, 0)) -> Config:
     c = Config()
     load().jacobi_config_default(ctypes.byref(c))
     c.strategy = STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
@@ -171,6 +173,7 @@ def make_config(strategy="sync", depth=1, tile=(0, 0), check_every=8,
     c.division = DIVISIONS[division] if isinstance(division, str) else int(division)
     c.rhs = RHS_MODES[rhs] if isinstance(rhs, str) else int(rhs)
     c.adapt = ADAPTS[adapt] if isinstance(adapt, str) else int(adapt)
+    c.overlap_x, c.overlap_y = int(overlap[0]), int(overlap[1])
     return c
 
 
@@ -205,7 +208,7 @@ class Solver:
     def __init__(self, u, u_alt, b, r, *, strategy="sync", depth=1,
                  tile=(0, 0), check_every=8, tol=1e-5, max_sweeps=1 << 22,
                  control="host", division="auto", rhs="fused", adapt="none",
-                 stream=None):
+                 overlap=(0, 0), stream=None):
         import torch
         lib = load()
         for t in (u, u_alt, b):
@@ -215,7 +218,7 @@ class Solver:
         self.stream = torch.cuda.current_stream(u.device) if stream is None else stream
         self._h = ctypes.c_void_p()
         cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
-                          control, division, rhs, adapt)
+                          control, division, rhs, adapt, overlap)
         with torch.cuda.device(u.device):
             rc = lib.jacobi_create(ctypes.byref(self._h), self.n, self.ld,
                                    float(r), ctypes.byref(cfg), _ptr(u),
@@ -260,9 +263,9 @@ class Solver:
 
     def set_strategy(self, strategy="sync", depth=1, tile=(0, 0),
                      check_every=8, tol=1e-5, max_sweeps=1 << 22, control="host",
-                     division="auto", rhs="fused", adapt="none"):
+                     division="auto", rhs="fused", adapt="none", overlap=(0, 0)):
         cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
-                          control, division, rhs, adapt)
+                          control, division, rhs, adapt, overlap)
         self._ok(load().jacobi_set_strategy(self.handle, ctypes.byref(cfg)))
         self.config = cfg
 

@@ -41,6 +41,13 @@ def test_invalid_arguments_rejected():
     with pytest.raises(jacobi.JacobiError) as e:  # tile_x not a multiple of 4
         jacobi.Solver(u, u_alt, b, 1.0, strategy="ba", depth=4, tile=(30, 8))
     assert e.value.status == jacobi.ERR_INVALID_ARG
+    for kw in (dict(strategy="ba", depth=4, overlap=(3, 0)),      # odd
+               dict(strategy="ba", depth=4, tile=(8, 8), overlap=(8, 0)),  # >= tile
+               dict(strategy="etb", depth=4, overlap=(2, 2)),     # not BA
+               dict(strategy="ba", depth=4, overlap=(-2, 0))):
+        with pytest.raises(jacobi.JacobiError) as e:
+            jacobi.Solver(u, u_alt, b, 1.0, **kw)
+        assert e.value.status == jacobi.ERR_INVALID_ARG, kw
     # misaligned (4-byte offset) view
     big = torch.zeros(32 * 32 + 4, device="cuda")
     mis = big[1:1 + 32 * 32].view(32, 32)

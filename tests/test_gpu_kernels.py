@@ -131,7 +131,7 @@ def test_etb_launch_equals_depth_sync_sweeps(n, depth, tile, division):
 
 
 @pytest.mark.parametrize("n", [17, 70, 130, 259])
-@pytest.mark.parametrize("depth", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("depth", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("tile", [(32, 8), (32, 16), (64, 32), (4, 3), (128, 64)])
 def test_block_async_launch_matches_emulator(n, depth, tile):
     """Block-asynchronous launch: tiles swept D times against halos frozen at
@@ -150,6 +150,34 @@ def test_block_async_launch_matches_emulator(n, depth, tile):
             assert same_bits(interior(got), interior(ref)), mismatch(got, ref)
         if depth == 1:
             assert same_bits(interior(ref), interior(oracle.sweeps(u0, b_ref, r, 2)))
+
+
+@pytest.mark.parametrize("n", [17, 70, 131, 259])
+@pytest.mark.parametrize("depth", [1, 4, 8, 16, 32])
+@pytest.mark.parametrize("tile,overlap", [
+    ((32, 8), (2, 2)), ((32, 8), (4, 0)), ((32, 32), (4, 4)),
+    ((16, 16), (6, 2)), ((8, 4), (2, 2)), ((64, 32), (30, 8)), ((4, 3), (2, 2)),
+])
+def test_block_async_overlap_matches_oracle(n, depth, tile, overlap):
+    """Overlapping subdomains ("Hierarchical Jacobi Iteration for Structured
+    Matrices on GPUs using Shared Memory"): tiles start every tile - overlap
+    cells and write back their half of each shared band; bit for bit against
+    the oracle's launch."""
+    r = 1.0 if depth < 8 else 10.0
+    u0, g = fields(n, 4, seed=11 * n + depth)
+    s, u, b = make_solver(u0, r, strategy="ba", depth=depth, tile=tile,
+                          overlap=overlap)
+    with s:
+        s.rhs(to_dev(g))
+        b_ref = oracle.rhs(u0, g)
+        ref = u0
+        for _ in range(2):
+            s.sweeps(1)
+            ref = oracle.ba_overlap_launch(ref, b_ref, r, tile[0], tile[1],
+                                           overlap[0], overlap[1], depth)
+            got = u.cpu().numpy()
+            assert same_bits(interior(got), interior(ref)), mismatch(got, ref)
+        assert np.isnan(got[:, n:]).all()
 
 
 @pytest.mark.parametrize("r", [1.0, 10.0, 100.0])

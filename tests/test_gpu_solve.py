@@ -94,6 +94,25 @@ def test_block_async_solve(n, r, source, depth, tile, control):
     assert np.abs(interior(got_u).astype(np.float64) - interior(sync_u)).max() <= 5e-4 * float(bmax)
 
 
+@pytest.mark.parametrize("control", CONTROLS)
+@pytest.mark.parametrize("n,r,source,depth,tile,overlap", [
+    (130, 10.0, "gauss", 8, (32, 32), (4, 4)),
+    (259, 100.0, "point", 16, (32, 16), (4, 2)),
+    (70, 1.0, "gauss", 4, (16, 8), (2, 2)),
+])
+def test_block_async_overlap_solve(n, r, source, depth, tile, overlap, control):
+    u0, g = workload(n, source)
+    ref_u, ref_k, _ = oracle.run(u0, g, r, depth=depth, tile_x=tile[0],
+                                 tile_y=tile[1], overlap=overlap)
+    got_u, got_k, _ = gpu_run(u0, g, r, strategy="ba", depth=depth, tile=tile,
+                              overlap=overlap, control=control)
+    assert got_k == ref_k
+    assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
+    sync_u, _, sync_b = oracle.run(u0, g, r)
+    _, bmax = oracle.residual(sync_u, sync_b, r)
+    assert np.abs(interior(got_u).astype(np.float64) - interior(sync_u)).max() <= 5e-4 * float(bmax)
+
+
 def test_block_async_depth1_equals_sync():
     u0, g = workload(200, "gauss")
     a_u, a_k, _ = gpu_run(u0, g, 10.0, strategy="ba", depth=1)
