@@ -27,9 +27,7 @@ struct jacobi_handle {
     cudaStream_t stream = nullptr;   // caller's stream: all work goes here
     cudaStream_t capture = nullptr;  // private stream used to record graphs
 
-    // Library-owned device scratch.
-    float *partials = nullptr;     // 2 words per reduction block
-    size_t partial_blocks = 0;     // capacity of `partials` in blocks
+    // Library-owned device state.
     ResidualOut *dev_out = nullptr;
     ResidualOut *host_out = nullptr;  // pinned
     LoopState *loop = nullptr;        // device-side loop state
@@ -220,7 +218,7 @@ LaunchCtl loop_ctl(jacobi_handle_t *h, bool fused, int src_is_alt,
     c.stop = &h->loop->stop;
     c.fused = fused;
     c.lp.state = h->loop;
-    c.lp.partials = reinterpret_cast<unsigned *>(h->partials);
+    c.lp.d = h->g.d;
     c.lp.tol = h->cfg.tol;
     c.lp.max_sweeps = h->cfg.max_sweeps;
     c.lp.interval = h->interval;
@@ -282,8 +280,8 @@ int record_batch(jacobi_handle_t *h, int start, cudaGraphExec_t *exec) {
         src ^= 1;
     }
     if (e == cudaSuccess)
-        e = launch_residual(h->g, src ? h->u_alt : h->u, h->b, h->partials,
-                            h->dev_out, 0, h->cfg.tol, h->capture);
+        e = launch_residual(h->g, src ? h->u_alt : h->u, h->b, h->dev_out,
+                            h->capture);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(h->host_out, h->dev_out, sizeof(ResidualOut),
                             cudaMemcpyDeviceToHost, h->capture);
@@ -309,15 +307,15 @@ long long intervals_per_iteration(long long launches_per_check) {
 }
 
 // Device control: record the graph of one time step,
-//   reset(LoopState) -> WHILE(cond) { body } -> copy LoopState to the host,
+//   reset(LoopState) -> bmax of b -> WHILE(cond) { body } -> copy LoopState
+//   to the host,
 // where the body is intervals_per_iteration() check intervals starting from u,
 // each with a fused first launch and the rest honouring the stop flag.
 int record_step(jacobi_handle_t *h) {
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaGraphCreate(&graph, 0);
     cudaGraphConditionalHandle cond{};
-    cudaGraphNode_t reset_node = nullptr, loop_node = nullptr;
-    size_t count = 1;
+    cudaGraphNode_t head_node = nullptr, loop_node = nullptr;
     const long long L = h->launches_per_check;
     const long long halves = intervals_per_iteration(L);
     auto check = [&](cudaError_t err) {
@@ -330,9 +328,19 @@ int record_step(jacobi_handle_t *h) {
         check(cudaStreamBeginCaptureToGraph(h->capture, graph, nullptr, nullptr,
                                             0, cudaStreamCaptureModeThreadLocal))) {
         check(launch_loop_reset(h->loop, h->capture));
+        // bmax of the step's right-hand side, once per step (b is fixed).
+        check(launch_bnorm(h->g, h->u, h->b, h->loop, h->capture));
+        // The loop node follows the last node captured so far.
+        cudaStreamCaptureStatus cs;
+        const cudaGraphNode_t *deps = nullptr;
+        size_t ndeps = 0;
+        if (check(cudaStreamGetCaptureInfo(h->capture, &cs, nullptr, nullptr,
+                                           &deps, nullptr, &ndeps))) {
+            if (ndeps == 1) head_node = deps[0];
+            else check(cudaErrorStreamCaptureUnmatched);
+        }
         cudaGraph_t g2 = nullptr;
         check(cudaStreamEndCapture(h->capture, &g2));
-        check(cudaGraphGetNodes(graph, &reset_node, &count));
     }
     cudaGraph_t body = nullptr;
     if (e == cudaSuccess) {
@@ -341,7 +349,7 @@ int record_step(jacobi_handle_t *h) {
         p.conditional.handle = cond;
         p.conditional.type = cudaGraphCondTypeWhile;
         p.conditional.size = 1;
-        if (check(cudaGraphAddNode(&loop_node, graph, &reset_node, nullptr, 1, &p)))
+        if (check(cudaGraphAddNode(&loop_node, graph, &head_node, nullptr, 1, &p)))
             body = p.conditional.phGraph_out[0];
     }
     if (e == cudaSuccess &&
@@ -354,6 +362,7 @@ int record_step(jacobi_handle_t *h) {
                                      loop_ctl(h, l == 0, src, cond)));
                 src ^= 1;
             }
+        check(launch_loop_condition(h->loop, cond, h->capture));
         cudaGraph_t g2 = nullptr;
         check(cudaStreamEndCapture(h->capture, &g2));
     }
@@ -373,20 +382,6 @@ int record_step(jacobi_handle_t *h) {
         return fail(h, JACOBI_ERR_CUDA, "recording the device-loop graph: %s",
                     cudaGetErrorString(e));
     }
-    return JACOBI_OK;
-}
-
-// Make sure `partials` holds at least `blocks` reductions' worth of words.
-int ensure_partials(jacobi_handle_t *h, size_t blocks) {
-    if (blocks <= h->partial_blocks) return JACOBI_OK;
-    if (h->partials) {
-        cudaStreamSynchronize(h->stream);
-        cudaFree(h->partials);
-        h->partials = nullptr;
-        h->partial_blocks = 0;
-    }
-    TBJ_CUDA(h, cudaMalloc(&h->partials, sizeof(float) * 2 * blocks));
-    h->partial_blocks = blocks;
     return JACOBI_OK;
 }
 
@@ -480,12 +475,6 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     h->interval = (long long)c.check_every /
                   gcd_ll(c.check_every, h->per_launch) * h->per_launch;
     h->launches_per_check = h->interval / h->per_launch;
-    size_t blocks = (size_t)residual_blocks(h->g);
-    const size_t sweep_blocks = c.strategy == JACOBI_SYNC
-                                    ? (size_t)sweep_sync_blocks(h->g)
-                                    : (size_t)tiled_blocks(h->g, h->tc);
-    if (sweep_blocks > blocks) blocks = sweep_blocks;
-    if ((rc = ensure_partials(h, blocks))) return rc;
     if (c.control == JACOBI_CONTROL_DEVICE) return record_step(h);
     if ((rc = record_batch(h, 0, &h->batch[0]))) return rc;
     if (h->launches_per_check % 2 == 1)
@@ -676,7 +665,8 @@ static long long solve_step_device(jacobi_handle_t *h) {
     const long long checks = st.result_k / h->interval + 1;
     const long long per_body = intervals_per_iteration(h->launches_per_check);
     const long long iters = (checks + per_body - 1) / per_body;
-    h->launches += 1 + iters * per_body * h->launches_per_check;
+    // reset + bmax, then per iteration the body and its condition kernel
+    h->launches += 2 + iters * (per_body * h->launches_per_check + 1);
     if (!st.stop)
         return fail(h, JACOBI_ERR_CUDA, "device loop ended without a decision");
     h->cur = st.where;
@@ -842,8 +832,7 @@ int jacobi_residual(jacobi_handle_t *h, float *rmax, float *bmax) {
     if (int rc0 = check_b_mode(h)) return rc0;
     int rc = settle(h);
     if (rc) return rc;
-    TBJ_CUDA(h, launch_residual(h->g, h->u, h->b, h->partials, h->dev_out, 0,
-                                h->cfg.tol, h->stream));
+    TBJ_CUDA(h, launch_residual(h->g, h->u, h->b, h->dev_out, h->stream));
     h->launches += 1;
     TBJ_CUDA(h, cudaMemcpyAsync(h->host_out, h->dev_out, sizeof(ResidualOut),
                                 cudaMemcpyDeviceToHost, h->stream));
@@ -904,7 +893,6 @@ void jacobi_destroy(jacobi_handle_t *h) {
     for (auto &e : h->ev)
         if (e) cudaEventDestroy(e);
     if (h->capture) cudaStreamDestroy(h->capture);
-    if (h->partials) cudaFree(h->partials);
     if (h->dev_out) cudaFree(h->dev_out);
     if (h->host_out) cudaFreeHost(h->host_out);
     if (h->loop) cudaFree(h->loop);

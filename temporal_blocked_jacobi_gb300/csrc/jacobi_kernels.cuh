@@ -101,23 +101,29 @@ struct ResidualOut {
     float bmax;
     unsigned err;       // OR of ERR_* bits seen since the last reset
     unsigned ticket;    // last-block counter, returns to 0 after each use
+    unsigned racc, bacc;  // running maxima (bit patterns); 0 between uses
 };
 
 // ---------------------------------------------------------------------------
 // Device-side convergence loop.
 //
-// With JACOBI_CONTROL_DEVICE a whole time step is one graph: a conditional
-// WHILE node repeats the check interval. The first launch of each interval
-// is "fused": besides its sweeps it computes the residual norms of its INPUT
-// iterate (rmax = max d|J(u)-u|, bmax = max |b_I|, exactly as k_residual
-// does, since its first sweep evaluates J(u) anyway), and the last of its
-// blocks to finish applies the stopping rule, updates LoopState and sets the
-// loop condition. Every launch first reads LoopState::stop and returns at
-// once when it is set, so launches queued after the stop do nothing and the
-// answer (the fused launch's input) is left intact.
+// With JACOBI_CONTROL_DEVICE a whole time step is one graph: a reset, the
+// right-hand-side norm bmax = max |b_I| of the step (b does not change
+// within a step), then a conditional WHILE node that repeats the check
+// interval. The first launch of each interval is "fused": besides its sweeps
+// it reduces max |J(u) - u| over its INPUT iterate (its first sweep evaluates
+// J(u) anyway) into LoopState::rbits with one atomicMax per block, and the
+// last of its blocks to finish forms rmax = d * that maximum (the same value
+// as the maximum of d|J(u) - u| cell by cell: rounding is monotone), applies
+// the stopping rule and updates LoopState. A small kernel at the end of each
+// loop iteration clears the loop condition once LoopState::stop is set.
+// Every launch first reads LoopState::stop and returns at once when it is
+// set, so launches queued after the stop do nothing and the answer (the
+// fused launch's input) is left intact.
 // ---------------------------------------------------------------------------
 struct LoopState {
-    float rmax, bmax;     // norms at the last check
+    float rmax;           // rmax at the last check
+    float bmax;           // bmax of the step's right-hand side
     unsigned err;         // ERR_* bits
     unsigned ticket;      // last-block counter of the fused reduction
     long long k;          // sweeps done before the current check interval
@@ -125,12 +131,13 @@ struct LoopState {
     int stop;             // 1 once the step has finished
     int status;           // 0 converged, or a negative jacobi_status_t
     int where;            // buffer holding the answer: 0 u, 1 u_alt
-    int pad;
+    unsigned rbits;       // running max of |J(u) - u| (bit pattern) of the
+                          // current check; 0 between checks
 };
 
 struct LoopParams {
     LoopState *state;
-    unsigned *partials;      // 2 words per block of the fused launch
+    float d;                 // 1 + 4r: rmax = d * max |J(u) - u|
     double tol;
     long long max_sweeps;
     long long interval;      // sweeps per check interval
@@ -191,90 +198,42 @@ __device__ __forceinline__ void loop_decide(const LoopParams &lp, float rmax,
     } else {
         st->k = k + lp.interval;
     }
-    cudaGraphSetConditional(lp.cond, stop ? 0u : 1u);
 }
 
-// Block-level end of a fused launch: reduce (rm, bm) over the block, publish
-// the block's partials, and let the last block reduce all partials and apply
-// the stopping rule. Every block of a fused launch must call this exactly
-// once (blocks with no cells pass zeros). `scratch` is __shared__ space for
-// 2 * 32 + 1 words.
-__device__ __forceinline__ void fused_block_finish(unsigned rm, unsigned bm,
+// Block-level end of a fused launch: reduce the block's max |J(u) - u| bits
+// rm, fold it into LoopState::rbits, and let the last block to finish form
+// rmax = d * max and apply the stopping rule with the step's bmax. Every
+// block of a fused launch must call this exactly once (blocks with no cells
+// pass 0). `scratch` is __shared__ space for 32 + 1 words.
+__device__ __forceinline__ void fused_block_finish(unsigned rm,
                                                    const LoopParams &lp,
                                                    unsigned *scratch) {
     const int tid = threadIdx.x + threadIdx.y * blockDim.x;
     const int nthreads = blockDim.x * blockDim.y;
     const int lane = tid & 31, warp = tid >> 5, nwarps = (nthreads + 31) >> 5;
-    unsigned *s_r = scratch, *s_b = scratch + 32;
-    unsigned *s_last = scratch + 64;
     rm = warp_max_u(rm);
-    bm = warp_max_u(bm);
     __syncthreads();  // scratch may alias memory the block used before
-    if (lane == 0) {
-        s_r[warp] = rm;
-        s_b[warp] = bm;
-    }
+    if (lane == 0) scratch[warp] = rm;
     __syncthreads();
-    const unsigned nblocks = gridDim.x * gridDim.y;
-    const unsigned bid = blockIdx.y * gridDim.x + blockIdx.x;
-    if (tid == 0) {
-        unsigned br = 0u, bb = 0u;
-        for (int w = 0; w < nwarps; ++w) {
-            br = max(br, s_r[w]);
-            bb = max(bb, s_b[w]);
-        }
-        lp.partials[2 * bid] = br;
-        lp.partials[2 * bid + 1] = bb;
-        __threadfence();
-        const unsigned t = atomicAdd(&lp.state->ticket, 1u);
-        *s_last = (t == nblocks - 1) ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!*s_last) return;
+    if (tid != 0) return;
+    unsigned br = 0u;
+    for (int w = 0; w < nwarps; ++w) br = max(br, scratch[w]);
+    LoopState *st = lp.state;
+    if (br) atomicMax(&st->rbits, br);
     __threadfence();
-    rm = 0u;
-    bm = 0u;
-    const volatile unsigned *vp = lp.partials;
-    for (unsigned k = tid; k < nblocks; k += nthreads) {
-        rm = max(rm, vp[2 * k]);
-        bm = max(bm, vp[2 * k + 1]);
-    }
-    rm = warp_max_u(rm);
-    bm = warp_max_u(bm);
-    __syncthreads();
-    if (lane == 0) {
-        s_r[warp] = rm;
-        s_b[warp] = bm;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        unsigned br = 0u, bb = 0u;
-        for (int w = 0; w < nwarps; ++w) {
-            br = max(br, s_r[w]);
-            bb = max(bb, s_b[w]);
-        }
-        lp.state->ticket = 0u;
-        loop_decide(lp, __uint_as_float(br), __uint_as_float(bb));
-    }
+    const unsigned nblocks = gridDim.x * gridDim.y;
+    if (atomicAdd(&st->ticket, 1u) != nblocks - 1) return;
+    // Last block: every other block's atomicMax is visible.
+    __threadfence();
+    const unsigned bits = atomicExch(&st->rbits, 0u);
+    st->ticket = 0u;
+    // max_i fl(d |x_i|) = fl(d max_i |x_i|): rounding is monotone.
+    loop_decide(lp, __fmul_rn(lp.d, __uint_as_float(bits)), st->bmax);
 }
 
-// Residual contributions of one interior cell (i, x) whose new value nv =
-// J(u) was just computed from centre c and neighbours w, e, n_, s_:
-// e = d|nv - c| and |b_I| with the Dirichlet-ring neighbours folded in.
-__device__ __forceinline__ void cell_residual(float nv, float c, float w,
-                                              float e, float n_, float s_,
-                                              float bb, int i, int x, int n,
-                                              float r, float d, unsigned &rm,
-                                              unsigned &bm) {
-    const float res = __fmul_rn(d, fabsf(__fsub_rn(nv, c)));
-    const float qw = (x - 1 == 0) ? w : 0.f;
-    const float qe = (x + 1 == n - 1) ? e : 0.f;
-    const float qn = (i - 1 == 0) ? n_ : 0.f;
-    const float qs = (i + 1 == n - 1) ? s_ : 0.f;
-    const float q = __fadd_rn(__fadd_rn(qw, qe), __fadd_rn(qn, qs));
-    const float bi = __fadd_rn(bb, __fmul_rn(r, q));
-    rm = max(rm, abs_bits(res));
-    bm = max(bm, abs_bits(bi));
+// |J(u) - u| of one cell as an orderable bit pattern (NaN above +Inf).
+__device__ __forceinline__ unsigned change_bits(float nv, float c) {
+    return abs_bits(__fsub_rn(nv, c));
 }
 
 // ---------------------------------------------------------------------------
@@ -319,12 +278,19 @@ cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
                               const LaunchCtl &ctl, cudaStream_t stream);
 int sweep_sync_blocks(const GridDesc &g);
 cudaError_t launch_loop_reset(LoopState *st, cudaStream_t stream);
-// partials: 2 * residual_blocks(g) floats of scratch.
-int residual_blocks(const GridDesc &g);
+// End of a loop iteration: clear the loop condition once LoopState::stop is
+// set. The sweep kernels only set the flag; keeping the graph call in this
+// one small kernel keeps it out of the sweep kernels.
+cudaError_t launch_loop_condition(const LoopState *st,
+                                  cudaGraphConditionalHandle cond,
+                                  cudaStream_t stream);
+// Residual norms of u into *out (rmax, bmax; out->racc, bacc and ticket
+// must be 0, as they are after every use).
 cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
-                            float *partials, ResidualOut *out,
-                            cudaGraphConditionalHandle cond, double tol,
-                            cudaStream_t stream);
+                            ResidualOut *out, cudaStream_t stream);
+// bmax of the step's right-hand side into st->bmax (which must be 0).
+cudaError_t launch_bnorm(const GridDesc &g, const float *u, const float *b,
+                         LoopState *st, cudaStream_t stream);
 
 // Tiled strategies (TMA-staged). Box = tile plus halo, read through the
 // tensor maps of the source field and of b.

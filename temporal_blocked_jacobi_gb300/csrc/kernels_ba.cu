@@ -128,7 +128,7 @@ __device__ __forceinline__ void ba_sweeps(const float *sA, float *sB, float *sC,
                                           long long ld, float r, float d,
                                           float y, int depth, int tx, int ty,
                                           int sx, int sy, int bxo, int byo,
-                                          unsigned &rm, unsigned &bm) {
+                                          unsigned &rm) {
     constexpr int BX = 128 * CH;
     const int lane = threadIdx.x & 31;
     const int r0 = 1 + (threadIdx.x >> 5) * RW;  // first box row of the band
@@ -208,16 +208,14 @@ __device__ __forceinline__ void ba_sweeps(const float *sA, float *sB, float *sC,
                     float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w, e,
                                               ex, wy, r, d, y);
                     if (FUSED && s == 0 && row_ok) {
-                        // Residual of the launch's input (sweep 0 reads A,
+                        // |J(u) - u| of the launch's input (sweep 0 reads A,
                         // so nv = J(u)) at this super-tile's cells.
-                        const float4 c4 = cr[c], n4 = nr[c], s4 = sr[c];
-                        const float4 b4 = breg[j][c];
-                        const int gx = bxo + 128 * c + col;
+                        const float4 c4 = cr[c];
                         const unsigned m = keep[c];
-                        if (m & 1u) cell_residual(nv.x, c4.x, w, ex, n4.x, s4.x, b4.x, gy, gx + 0, n, r, d, rm, bm);
-                        if (m & 2u) cell_residual(nv.y, c4.y, wy, c4.z, n4.y, s4.y, b4.y, gy, gx + 1, n, r, d, rm, bm);
-                        if (m & 4u) cell_residual(nv.z, c4.z, c4.y, c4.w, n4.z, s4.z, b4.z, gy, gx + 2, n, r, d, rm, bm);
-                        if (m & 8u) cell_residual(nv.w, c4.w, c4.z, e, n4.w, s4.w, b4.w, gy, gx + 3, n, r, d, rm, bm);
+                        if (m & 1u) rm = max(rm, change_bits(nv.x, c4.x));
+                        if (m & 2u) rm = max(rm, change_bits(nv.y, c4.y));
+                        if (m & 4u) rm = max(rm, change_bits(nv.z, c4.z));
+                        if (m & 8u) rm = max(rm, change_bits(nv.w, c4.w));
                     }
                     if (EDGE) nv = hold4(nv, cr[c], row_ok, interior[c]);
                     if (!last) {
@@ -250,7 +248,7 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
      int sy, unsigned *err, const int *stop, LoopParams lp) {
     constexpr int BX = 128 * CH;
     constexpr int ROWS = kRowsMax + 2;
-    __shared__ unsigned fin_scratch[65];
+    __shared__ unsigned fin_scratch[33];
     allow_dependents();
     const int bxo = blockIdx.x * sx;  // grid coords of box cell (0,0)
     const int byo = blockIdx.y * sy;
@@ -285,7 +283,7 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
     if (__syncthreads_or(!ok)) {
         if (tid == 0) atomicOr(err, (unsigned)ERR_TMA_TIMEOUT);
         mbar_wait_bounded(bar);
-        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
+        if (FUSED) fused_block_finish(0u, lp, fin_scratch);
         return;
     }
     const int lane = tid & 31;
@@ -299,18 +297,18 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();  // C is first written by sweep 1, after a barrier
 
-    unsigned rm = 0u, bm = 0u;
+    unsigned rm = 0u;
     const bool edge = bxo < 1 || byo < 1 || bxo + BX > n - 1 ||
                       byo + sy + 2 > n - 1;
     if (edge)
         ba_sweeps<CH, RW, NW, FAST, true, FUSED>(sA, sB, sC, breg, out, n, ld, r,
                                                  d, y, depth, tx, ty, sx, sy, bxo,
-                                                 byo, rm, bm);
+                                                 byo, rm);
     else
         ba_sweeps<CH, RW, NW, FAST, false, FUSED>(sA, sB, sC, breg, out, n, ld, r,
                                                   d, y, depth, tx, ty, sx, sy, bxo,
-                                                  byo, rm, bm);
-    if (FUSED) fused_block_finish(rm, bm, lp, fin_scratch);
+                                                  byo, rm);
+    if (FUSED) fused_block_finish(rm, lp, fin_scratch);
 }
 
 template <int CH>

@@ -162,7 +162,7 @@ __device__ __forceinline__ void etb_sweeps(float *sA, float *sB,
                                            float *__restrict__ out, int n,
                                            long long ld, float r, float d,
                                            float y, int bxo, int byo,
-                                           unsigned &rm, unsigned &bm) {
+                                           unsigned &rm) {
     using S = EtbShape<D, CH, RW, NW>;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -224,26 +224,14 @@ __device__ __forceinline__ void etb_sweeps(float *sA, float *sB,
                     float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w,
                                               e, r, d, y);
                     if (FUSED && s == 0 && in_tile[c] && tile_row && row_ok) {
-                        // Residual of the launch's input at the tile's cells.
-                        const float4 c4 = cr[c], n4 = nr[c], s4 = sr[c];
-                        const float4 b4 = breg[j][c];
-                        if (EDGE) {
-                            const int gx = bxo + 128 * c + col;
-                            if (colmask[c] & 1u) cell_residual(nv.x, c4.x, w, c4.y, n4.x, s4.x, b4.x, gy, gx + 0, n, r, d, rm, bm);
-                            if (colmask[c] & 2u) cell_residual(nv.y, c4.y, c4.x, c4.z, n4.y, s4.y, b4.y, gy, gx + 1, n, r, d, rm, bm);
-                            if (colmask[c] & 4u) cell_residual(nv.z, c4.z, c4.y, c4.w, n4.z, s4.z, b4.z, gy, gx + 2, n, r, d, rm, bm);
-                            if (colmask[c] & 8u) cell_residual(nv.w, c4.w, c4.z, e, n4.w, s4.w, b4.w, gy, gx + 3, n, r, d, rm, bm);
-                        } else {
-                            // No ring cell is next to these cells: b_I = b.
-                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.x, c4.x)))));
-                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.y, c4.y)))));
-                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.z, c4.z)))));
-                            rm = max(rm, abs_bits(__fmul_rn(d, fabsf(__fsub_rn(nv.w, c4.w)))));
-                            bm = max(bm, abs_bits(b4.x));
-                            bm = max(bm, abs_bits(b4.y));
-                            bm = max(bm, abs_bits(b4.z));
-                            bm = max(bm, abs_bits(b4.w));
-                        }
+                        // |J(u) - u| of the launch's input at the tile's
+                        // interior cells.
+                        const float4 c4 = cr[c];
+                        const unsigned m = colmask[c];
+                        if (m & 1u) rm = max(rm, change_bits(nv.x, c4.x));
+                        if (m & 2u) rm = max(rm, change_bits(nv.y, c4.y));
+                        if (m & 4u) rm = max(rm, change_bits(nv.z, c4.z));
+                        if (m & 8u) rm = max(rm, change_bits(nv.w, c4.w));
                     }
                     if (EDGE) nv = hold4(nv, cr[c], row_ok, colmask[c]);
                     if (!last) {
@@ -296,7 +284,7 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
       const int *stop, LoopParams lp, int tiles_x, int tiles) {
     using S = EtbShape<D, CH, RW, NW, NB>;
     static_assert(S::SMEM <= 227 * 1024, "shared memory per block");
-    __shared__ unsigned fin_scratch[65];
+    __shared__ unsigned fin_scratch[33];
     allow_dependents();
 
     // Offsets from the __shared__ array itself, so that every access stays
@@ -330,7 +318,7 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
 
     const int lane = tid & 31;
     const int band = (tid >> 5) * RW;
-    unsigned rm = 0u, bm = 0u;
+    unsigned rm = 0u;
     bool failed = false;
     int fail_p = 0;
     unsigned fail_parity = 0u;
@@ -369,11 +357,10 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
                           byo + S::BY > n - 1;
         if (edge)
             etb_sweeps<D, CH, RW, NW, FAST, true, FUSED>(sA, sB, breg, out, n, ld,
-                                                         r, d, y, bxo, byo, rm, bm);
+                                                         r, d, y, bxo, byo, rm);
         else
             etb_sweeps<D, CH, RW, NW, FAST, false, FUSED>(sA, sB, breg, out, n,
-                                                          ld, r, d, y, bxo, byo, rm,
-                                                          bm);
+                                                          ld, r, d, y, bxo, byo, rm);
         if (NB == 1 && t + (int)gridDim.x < tiles) {
             __syncthreads();  // everyone is done with the single buffer set
             if (tid == 0) {
@@ -390,7 +377,7 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
         // is released.
         mbar_wait_parity(&bars[fail_p], fail_parity);
     }
-    if (FUSED) fused_block_finish(rm, bm, lp, fin_scratch);
+    if (FUSED) fused_block_finish(rm, lp, fin_scratch);
 }
 
 // Shapes per depth: {CH, RW, NW, NB}. The first one of a depth is its

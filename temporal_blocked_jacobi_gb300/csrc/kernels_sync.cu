@@ -106,7 +106,7 @@ k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
     const bool active = x0 < n;
     const int i0 = 1 + (blockIdx.y * kWarps + threadIdx.y) * ROWS;
     const int i1 = min(i0 + ROWS, n - 1);
-    unsigned rm = 0u, bm = 0u;
+    unsigned rm = 0u;  // fused: max |J(u) - u| bits
     if (i0 <= n - 2) {  // uniform across the warp
         float4 top = make_float4(0.f, 0.f, 0.f, 0.f), mid = top;
         if (active) {
@@ -130,14 +130,10 @@ k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
             if (active) {
                 store_interior(out + (long long)i * ld, x0, n, o);
                 if (FUSED) {
-                    if (x0 + 0 >= 1 && x0 + 0 <= n - 2)
-                        cell_residual(o.x, mid.x, west, mid.y, top.x, cur.bot.x, cur.bb.x, i, x0 + 0, n, r, d, rm, bm);
-                    if (x0 + 1 >= 1 && x0 + 1 <= n - 2)
-                        cell_residual(o.y, mid.y, mid.x, mid.z, top.y, cur.bot.y, cur.bb.y, i, x0 + 1, n, r, d, rm, bm);
-                    if (x0 + 2 >= 1 && x0 + 2 <= n - 2)
-                        cell_residual(o.z, mid.z, mid.y, mid.w, top.z, cur.bot.z, cur.bb.z, i, x0 + 2, n, r, d, rm, bm);
-                    if (x0 + 3 >= 1 && x0 + 3 <= n - 2)
-                        cell_residual(o.w, mid.w, mid.z, east, top.w, cur.bot.w, cur.bb.w, i, x0 + 3, n, r, d, rm, bm);
+                    if (x0 + 0 >= 1 && x0 + 0 <= n - 2) rm = max(rm, change_bits(o.x, mid.x));
+                    if (x0 + 1 >= 1 && x0 + 1 <= n - 2) rm = max(rm, change_bits(o.y, mid.y));
+                    if (x0 + 2 >= 1 && x0 + 2 <= n - 2) rm = max(rm, change_bits(o.z, mid.z));
+                    if (x0 + 3 >= 1 && x0 + 3 <= n - 2) rm = max(rm, change_bits(o.w, mid.w));
                 }
             }
             top = mid;
@@ -145,8 +141,8 @@ k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
         }
     }
     if (FUSED) {
-        __shared__ unsigned scratch[65];
-        fused_block_finish(rm, bm, lp, scratch);
+        __shared__ unsigned scratch[33];
+        fused_block_finish(rm, lp, scratch);
     }
 }
 
@@ -158,9 +154,9 @@ k_sweep_sync(const float *__restrict__ u, const float *__restrict__ b,
 //        unknowns)
 // rmax = max e, bmax = max |bI|. Maxima are taken on the IEEE bit patterns
 // of non-negative floats, which order like the values and put NaN above
-// +Inf, so a NaN anywhere reaches the result. Each block writes its two
-// maxima to `partials`; the last block to finish reduces them, writes `out`
-// and re-arms the ticket.
+// +Inf, so a NaN anywhere reaches the result. Each block folds its two
+// maxima into out->racc / bacc with atomicMax; the last block to finish
+// (ticket) moves them to out->rmax / bmax and re-arms the accumulators.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ unsigned fbits(float x) {
     return __float_as_uint(fabsf(x));
@@ -195,8 +191,7 @@ template <int ROWS, bool FAST, bool UNF>
 __global__ void __launch_bounds__(32 * kWarps)
 k_residual(const float *__restrict__ u, const float *__restrict__ b,
            const float *__restrict__ g, int n, long long ld, float r, float d,
-           float y, unsigned *__restrict__ partials,
-           ResidualOut *__restrict__ out) {
+           float y, ResidualOut *__restrict__ out) {
     const int lane = threadIdx.x;
     const int vx = blockIdx.x * 32 + lane;
     const int x0 = vx * 4;
@@ -232,56 +227,62 @@ k_residual(const float *__restrict__ u, const float *__restrict__ b,
     rm = warp_max(rm);
     bm = warp_max(bm);
     __shared__ unsigned s_r[kWarps], s_b[kWarps];
-    __shared__ bool s_last;
     if (lane == 0) {
         s_r[threadIdx.y] = rm;
         s_b[threadIdx.y] = bm;
     }
     __syncthreads();
-    const unsigned nblocks = gridDim.x * gridDim.y;
-    const unsigned bid = blockIdx.y * gridDim.x + blockIdx.x;
-    if (threadIdx.y == 0 && lane == 0) {
-        unsigned br = 0u, bbm = 0u;
-        for (int w = 0; w < kWarps; ++w) {
-            br = max(br, s_r[w]);
-            bbm = max(bbm, s_b[w]);
-        }
-        partials[2 * bid] = br;
-        partials[2 * bid + 1] = bbm;
-        __threadfence();
-        const unsigned t = atomicAdd(&out->ticket, 1u);
-        s_last = (t == nblocks - 1);
+    if (threadIdx.y != 0 || lane != 0) return;
+    unsigned br = 0u, bbm = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+        br = max(br, s_r[w]);
+        bbm = max(bbm, s_b[w]);
     }
-    __syncthreads();
-    if (!s_last) return;
-    // Last block: reduce all partials.
+    if (br) atomicMax(&out->racc, br);
+    if (bbm) atomicMax(&out->bacc, bbm);
     __threadfence();
-    const int tid = threadIdx.y * 32 + lane;
-    rm = 0u;
-    bm = 0u;
-    const volatile unsigned *vp = partials;
-    for (unsigned k = tid; k < nblocks; k += 32 * kWarps) {
-        rm = max(rm, vp[2 * k]);
-        bm = max(bm, vp[2 * k + 1]);
-    }
-    rm = warp_max(rm);
-    bm = warp_max(bm);
-    __syncthreads();
-    if (lane == 0) {
-        s_r[threadIdx.y] = rm;
-        s_b[threadIdx.y] = bm;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        unsigned br = 0u, bbm = 0u;
-        for (int w = 0; w < kWarps; ++w) {
-            br = max(br, s_r[w]);
-            bbm = max(bbm, s_b[w]);
+    if (atomicAdd(&out->ticket, 1u) != gridDim.x * gridDim.y - 1) return;
+    // Last block: every other block's maxima are in.
+    __threadfence();
+    out->rmax = __uint_as_float(atomicExch(&out->racc, 0u));
+    out->bmax = __uint_as_float(atomicExch(&out->bacc, 0u));
+    out->ticket = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// bmax of a time step: max over the interior of |b_I|, b_I = b (+ g when the
+// right-hand side is unfused) + r * (the cell's Dirichlet-ring neighbours),
+// exactly as k_residual forms it. b is fixed within a step, so the
+// device-side loop takes it once per step. One block per row (grid-stride),
+// one atomicMax per block into st->bmax.
+// ---------------------------------------------------------------------------
+template <bool UNF>
+__global__ void __launch_bounds__(256)
+k_bnorm(const float *__restrict__ u, const float *__restrict__ b,
+        const float *__restrict__ g, int n, long long ld, float r,
+        LoopState *st) {
+    unsigned bm = 0u;
+    for (int i = 1 + blockIdx.x; i <= n - 2; i += gridDim.x) {
+        const long long row = (long long)i * ld;
+        for (int x = 1 + threadIdx.x; x <= n - 2; x += blockDim.x) {
+            const long long p = row + x;
+            float bb = b[p];
+            if (UNF) bb = __fadd_rn(bb, g[p]);
+            const float qw = (x == 1) ? u[p - 1] : 0.f;
+            const float qe = (x == n - 2) ? u[p + 1] : 0.f;
+            const float qn = (i == 1) ? u[p - ld] : 0.f;
+            const float qs = (i == n - 2) ? u[p + ld] : 0.f;
+            const float q = __fadd_rn(__fadd_rn(qw, qe), __fadd_rn(qn, qs));
+            bm = max(bm, abs_bits(__fadd_rn(bb, __fmul_rn(r, q))));
         }
-        out->rmax = __uint_as_float(br);
-        out->bmax = __uint_as_float(bbm);
-        out->ticket = 0u;
     }
+    bm = warp_max(bm);
+    __shared__ unsigned s_b[8];
+    if ((threadIdx.x & 31) == 0) s_b[threadIdx.x >> 5] = bm;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) bm = max(bm, s_b[w]);
+    if (bm) atomicMax(reinterpret_cast<unsigned *>(&st->bmax), bm);
 }
 
 // ---------------------------------------------------------------------------
@@ -327,6 +328,14 @@ __global__ void k_loop_reset(LoopState *st) {
     st->stop = 0;
     st->status = 0;
     st->where = 0;
+    st->rbits = 0u;
+}
+
+// The loop condition starts at 1 with every launch of the step's graph, so
+// only the stop needs setting.
+__global__ void k_loop_condition(const LoopState *st,
+                                 cudaGraphConditionalHandle cond) {
+    if (st->stop) cudaGraphSetConditional(cond, 0u);
 }
 
 dim3 strip_grid(int n, int rows) {
@@ -399,21 +408,20 @@ cudaError_t launch_loop_reset(LoopState *st, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-int residual_blocks(const GridDesc &g) {
-    const dim3 grid = strip_grid(g.n, rows_per_warp(g.n));
-    return (int)(grid.x * grid.y);
+cudaError_t launch_loop_condition(const LoopState *st,
+                                  cudaGraphConditionalHandle cond,
+                                  cudaStream_t stream) {
+    k_loop_condition<<<1, 1, 0, stream>>>(st, cond);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
-                            float *partials, ResidualOut *out,
-                            cudaGraphConditionalHandle, double,
-                            cudaStream_t stream) {
+                            ResidualOut *out, cudaStream_t stream) {
     const int rows = rows_per_warp(g.n);
     const dim3 grid = strip_grid(g.n, rows), block(32, kWarps);
-    unsigned *part = reinterpret_cast<unsigned *>(partials);
 #define TBJ_RESID_K(R, F, UN)                                                 \
     k_residual<R, F, UN><<<grid, block, 0, stream>>>(u, b, g.g2, g.n, g.ld,   \
-                                                     g.r, g.d, g.y, part, out)
+                                                     g.r, g.d, g.y, out)
 #define TBJ_RESID(R)                                                          \
     case R:                                                                   \
         if (g.fast) {                                                         \
@@ -432,6 +440,16 @@ cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
     }
 #undef TBJ_RESID
 #undef TBJ_RESID_K
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bnorm(const GridDesc &g, const float *u, const float *b,
+                         LoopState *st, cudaStream_t stream) {
+    const int blocks = g.n - 2 < 2048 ? g.n - 2 : 2048;
+    if (g.g2)
+        k_bnorm<true><<<blocks, 256, 0, stream>>>(u, b, g.g2, g.n, g.ld, g.r, st);
+    else
+        k_bnorm<false><<<blocks, 256, 0, stream>>>(u, b, nullptr, g.n, g.ld, g.r, st);
     return cudaGetLastError();
 }
 

@@ -114,12 +114,12 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
               float y, TileGeom tg, unsigned *err, const int *stop,
               LoopParams lp) {
     if (stop && *stop) return;  // same value for every thread of the launch
-    __shared__ unsigned fin_scratch[65];
+    __shared__ unsigned fin_scratch[33];
     const int tx = tg.tx, ty = tg.ty, box_x = tg.box_x, box_y = tg.box_y;
     const int gx0 = 1 + blockIdx.x * tg.sx;  // tile's first cell (grid)
     const int gy0 = 1 + blockIdx.y * tg.sy;
     if (gx0 > n - 2 || gy0 > n - 2) {
-        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
+        if (FUSED) fused_block_finish(0u, lp, fin_scratch);
         return;
     }
     // Box origin: one cell up, and left to a 16-byte boundary.
@@ -159,7 +159,7 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
         // Let any copy still in flight land before the block's shared
         // memory is released (bounded as well).
         mbar_wait_bounded(bar);
-        if (FUSED) fused_block_finish(0u, 0u, lp, fin_scratch);
+        if (FUSED) fused_block_finish(0u, lp, fin_scratch);
         return;
     }
 
@@ -169,7 +169,7 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
     const int warp = tid >> 5, lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
 
-    unsigned rm = 0u, bm = 0u;
+    unsigned rm = 0u;
 #pragma unroll 1
     for (int s = 0; s < D; ++s) {
         const float *src = (s & 1) ? sB : sA;
@@ -188,9 +188,8 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
                 const float v = jacobi_update<FAST>(w, e, nn, ss, brow[bx], r, d, y);
                 const int gx = bxo + bx;
                 const bool own = own_row && gx >= wx0 && gx < wx1;
-                if (FUSED && s == 0 && own)  // residual of the launch's input
-                    cell_residual(v, row[bx], w, e, nn, ss, brow[bx], gy, gx,
-                                  n, r, d, rm, bm);
+                if (FUSED && s == 0 && own)  // |J(u) - u| of the launch's input
+                    rm = max(rm, change_bits(v, row[bx]));
                 if (last) {
                     if (own) out[(long long)gy * ld + gx] = v;
                 } else {
@@ -200,7 +199,7 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
         }
         if (!last) __syncthreads();
     }
-    if (FUSED) fused_block_finish(rm, bm, lp, fin_scratch);
+    if (FUSED) fused_block_finish(rm, lp, fin_scratch);
 }
 
 cudaError_t launch_tiled(const GridDesc &g, const TileConf &tc,

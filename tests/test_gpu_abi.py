@@ -169,8 +169,9 @@ def test_launch_count_grows():
 
 @pytest.mark.parametrize("strategy,depth", [("sync", 1), ("etb", 4), ("etb", 8)])
 def test_device_control_launch_count(strategy, depth):
-    """Device control: one graph per step holding a reset kernel and the loop
-    body; launches after the stop are counted (they run and return)."""
+    """Device control: one graph per step holding a reset kernel, the bmax
+    kernel and the loop body (its sweep launches and one loop-condition
+    kernel); launches after the stop are counted (they run and return)."""
     jacobi = _jacobi()
     n = 64
     u0, g = workload(n, "point")
@@ -189,4 +190,4 @@ def test_device_control_launch_count(strategy, depth):
             body += 1
         iters = -(-checks // body)
         copy = 1 if (L % 2 and checks % 2 == 0) else 0
-        assert s.launch_count - c0 == 1 + iters * body * L + copy
+        assert s.launch_count - c0 == 2 + iters * (body * L + 1) + copy
