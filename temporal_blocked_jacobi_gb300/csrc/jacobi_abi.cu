@@ -45,8 +45,15 @@ struct jacobi_handle {
     // Host control: graph for a check interval starting from u (index 0)
     // and from u_alt (index 1; only when launches_per_check is odd).
     cudaGraphExec_t batch[2] = {nullptr, nullptr};
-    // Device control: one graph per time step (conditional WHILE loop).
+    // Device control: one graph per time step (conditional WHILE loop), and
+    // one graph for a whole jacobi_run of run_steps steps with source run_g.
     cudaGraphExec_t step = nullptr;
+    cudaGraphExec_t run = nullptr;
+    const float *run_g = nullptr;
+    int run_steps = 0;
+    LoopState *run_states = nullptr;       // device, run_cap entries
+    LoopState *run_states_host = nullptr;  // pinned copy
+    int run_cap = 0;
     int cur = 0;  // 0: the iterate is in u; 1: in u_alt
 
     // Adaptive depth (BLOCK_ASYNC with a depth controller): one fixed-depth
@@ -212,12 +219,12 @@ LaunchCtl plain_ctl() {
 
 // Control of a launch inside the device-side loop: honours the stop flag;
 // a fused launch also reduces the residual of its input and decides.
-LaunchCtl loop_ctl(jacobi_handle_t *h, bool fused, int src_is_alt,
-                   cudaGraphConditionalHandle cond) {
+LaunchCtl loop_ctl(jacobi_handle_t *h, LoopState *st, bool fused,
+                   int src_is_alt, cudaGraphConditionalHandle cond) {
     LaunchCtl c = plain_ctl();
-    c.stop = &h->loop->stop;
+    c.stop = &st->stop;
     c.fused = fused;
-    c.lp.state = h->loop;
+    c.lp.state = st;
     c.lp.d = h->g.d;
     c.lp.tol = h->cfg.tol;
     c.lp.max_sweeps = h->cfg.max_sweeps;
@@ -265,6 +272,10 @@ void destroy_graphs(jacobi_handle_t *h) {
     }
     if (h->step) cudaGraphExecDestroy(h->step);
     h->step = nullptr;
+    if (h->run) cudaGraphExecDestroy(h->run);
+    h->run = nullptr;
+    h->run_g = nullptr;
+    h->run_steps = 0;
 }
 
 // Record the check interval starting from buffer `start` (0 = u, 1 = u_alt):
@@ -306,6 +317,26 @@ long long intervals_per_iteration(long long launches_per_check) {
     return (launches_per_check % 2 == 1 && k % 2 == 1) ? k + 1 : k;
 }
 
+// The body of the device-side loop for the step whose state is `st`, into
+// the stream being captured: intervals_per_iteration() check intervals
+// starting from u, each with a fused first launch and the rest honouring the
+// stop flag, then the kernel that ends the loop once the step has stopped.
+cudaError_t capture_body(jacobi_handle_t *h, LoopState *st,
+                         cudaGraphConditionalHandle cond) {
+    const long long L = h->launches_per_check;
+    const long long halves = intervals_per_iteration(L);
+    int src = 0;
+    cudaError_t e = cudaSuccess;
+    for (long long half = 0; half < halves && e == cudaSuccess; ++half)
+        for (long long l = 0; l < L && e == cudaSuccess; ++l) {
+            e = enqueue_launch(h, src, h->capture,
+                               loop_ctl(h, st, l == 0, src, cond));
+            src ^= 1;
+        }
+    if (e == cudaSuccess) e = launch_loop_condition(st, cond, h->capture);
+    return e;
+}
+
 // Device control: record the graph of one time step,
 //   reset(LoopState) -> bmax of b -> WHILE(cond) { body } -> copy LoopState
 //   to the host,
@@ -316,8 +347,6 @@ int record_step(jacobi_handle_t *h) {
     cudaError_t e = cudaGraphCreate(&graph, 0);
     cudaGraphConditionalHandle cond{};
     cudaGraphNode_t head_node = nullptr, loop_node = nullptr;
-    const long long L = h->launches_per_check;
-    const long long halves = intervals_per_iteration(L);
     auto check = [&](cudaError_t err) {
         if (e == cudaSuccess) e = err;
         return e == cudaSuccess;
@@ -327,7 +356,7 @@ int record_step(jacobi_handle_t *h) {
                                                cudaGraphCondAssignDefault)) &&
         check(cudaStreamBeginCaptureToGraph(h->capture, graph, nullptr, nullptr,
                                             0, cudaStreamCaptureModeThreadLocal))) {
-        check(launch_loop_reset(h->loop, h->capture));
+        check(launch_loop_reset(h->loop, nullptr, h->capture));
         // bmax of the step's right-hand side, once per step (b is fixed).
         check(launch_bnorm(h->g, h->u, h->b, h->loop, h->capture));
         // The loop node follows the last node captured so far.
@@ -355,14 +384,7 @@ int record_step(jacobi_handle_t *h) {
     if (e == cudaSuccess &&
         check(cudaStreamBeginCaptureToGraph(h->capture, body, nullptr, nullptr,
                                             0, cudaStreamCaptureModeThreadLocal))) {
-        int src = 0;
-        for (long long half = 0; half < halves; ++half)
-            for (long long l = 0; l < L; ++l) {
-                check(enqueue_launch(h, src, h->capture,
-                                     loop_ctl(h, l == 0, src, cond)));
-                src ^= 1;
-            }
-        check(launch_loop_condition(h->loop, cond, h->capture));
+        check(capture_body(h, h->loop, cond));
         cudaGraph_t g2 = nullptr;
         check(cudaStreamEndCapture(h->capture, &g2));
     }
@@ -382,6 +404,120 @@ int record_step(jacobi_handle_t *h) {
         return fail(h, JACOBI_ERR_CUDA, "recording the device-loop graph: %s",
                     cudaGetErrorString(e));
     }
+    return JACOBI_OK;
+}
+
+// Device control, whole run: one graph for `steps` time steps with source g
+// (section 01: a run is successive backward-Euler steps). Step s is
+//   right-hand side -> reset(state s) -> bmax -> WHILE(cond s) { body }
+//   [-> settle: answer back into u, when intervals have an odd launch count]
+// and a single copy of all steps' states to pinned memory ends the graph.
+// A step whose predecessor did not converge is skipped on the device.
+int record_run(jacobi_handle_t *h, const float *g, int steps) {
+    if (h->run) cudaGraphExecDestroy(h->run);
+    h->run = nullptr;
+    h->run_g = nullptr;
+    h->run_steps = 0;
+    if (steps > h->run_cap) {
+        if (h->run_states) cudaFree(h->run_states);
+        if (h->run_states_host) cudaFreeHost(h->run_states_host);
+        h->run_states = nullptr;
+        h->run_states_host = nullptr;
+        h->run_cap = 0;
+        TBJ_CUDA(h, cudaMalloc(&h->run_states, sizeof(LoopState) * steps));
+        TBJ_CUDA(h, cudaMallocHost(&h->run_states_host, sizeof(LoopState) * steps));
+        h->run_cap = steps;
+    }
+    const bool settle_needed = h->launches_per_check % 2 == 1;
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaGraphCreate(&graph, 0);
+    auto check = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+        return e == cudaSuccess;
+    };
+    cudaGraphNode_t prev = nullptr;  // last node of the previous step
+    for (int s = 0; s < steps && e == cudaSuccess; ++s) {
+        LoopState *st = h->run_states + s;
+        cudaGraphConditionalHandle cond{};
+        cudaGraphNode_t head = nullptr, loop_node = nullptr;
+        check(cudaGraphConditionalHandleCreate(&cond, graph, 1,
+                                               cudaGraphCondAssignDefault));
+        if (e == cudaSuccess &&
+            check(cudaStreamBeginCaptureToGraph(
+                h->capture, graph, prev ? &prev : nullptr, nullptr,
+                prev ? 1 : 0, cudaStreamCaptureModeThreadLocal))) {
+            if (h->cfg.rhs == JACOBI_RHS_UNFUSED) {
+                if (s == 0) check(launch_copy_interior(h->g, g, h->g_copy, h->capture));
+                check(launch_copy_interior(h->g, h->u, h->b, h->capture));
+            } else {
+                check(launch_rhs(h->g, h->u, g, h->b, h->capture));
+            }
+            check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture));
+            check(launch_bnorm(h->g, h->u, h->b, st, h->capture));
+            cudaStreamCaptureStatus cs;
+            const cudaGraphNode_t *deps = nullptr;
+            size_t ndeps = 0;
+            if (check(cudaStreamGetCaptureInfo(h->capture, &cs, nullptr, nullptr,
+                                               &deps, nullptr, &ndeps))) {
+                if (ndeps == 1) head = deps[0];
+                else check(cudaErrorStreamCaptureUnmatched);
+            }
+            cudaGraph_t g2 = nullptr;
+            check(cudaStreamEndCapture(h->capture, &g2));
+        }
+        cudaGraph_t body = nullptr;
+        if (e == cudaSuccess) {
+            cudaGraphNodeParams p = {};
+            p.type = cudaGraphNodeTypeConditional;
+            p.conditional.handle = cond;
+            p.conditional.type = cudaGraphCondTypeWhile;
+            p.conditional.size = 1;
+            if (check(cudaGraphAddNode(&loop_node, graph, &head, nullptr, 1, &p)))
+                body = p.conditional.phGraph_out[0];
+        }
+        if (e == cudaSuccess &&
+            check(cudaStreamBeginCaptureToGraph(h->capture, body, nullptr, nullptr,
+                                                0, cudaStreamCaptureModeThreadLocal))) {
+            check(capture_body(h, st, cond));
+            cudaGraph_t g2 = nullptr;
+            check(cudaStreamEndCapture(h->capture, &g2));
+        }
+        prev = loop_node;
+        if (settle_needed && e == cudaSuccess &&
+            check(cudaStreamBeginCaptureToGraph(h->capture, graph, &loop_node,
+                                                nullptr, 1,
+                                                cudaStreamCaptureModeThreadLocal))) {
+            check(launch_settle(h->g, st, h->u_alt, h->u, h->capture));
+            cudaStreamCaptureStatus cs;
+            const cudaGraphNode_t *deps = nullptr;
+            size_t ndeps = 0;
+            if (check(cudaStreamGetCaptureInfo(h->capture, &cs, nullptr, nullptr,
+                                               &deps, nullptr, &ndeps))) {
+                if (ndeps == 1) prev = deps[0];
+                else check(cudaErrorStreamCaptureUnmatched);
+            }
+            cudaGraph_t g2 = nullptr;
+            check(cudaStreamEndCapture(h->capture, &g2));
+        }
+    }
+    if (e == cudaSuccess &&
+        check(cudaStreamBeginCaptureToGraph(h->capture, graph, &prev, nullptr, 1,
+                                            cudaStreamCaptureModeThreadLocal))) {
+        check(cudaMemcpyAsync(h->run_states_host, h->run_states,
+                              sizeof(LoopState) * steps, cudaMemcpyDeviceToHost,
+                              h->capture));
+        cudaGraph_t g2 = nullptr;
+        check(cudaStreamEndCapture(h->capture, &g2));
+    }
+    if (e == cudaSuccess) check(cudaGraphInstantiate(&h->run, graph, 0));
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, JACOBI_ERR_CUDA, "recording the run graph: %s",
+                    cudaGetErrorString(e));
+    }
+    h->run_g = g;
+    h->run_steps = steps;
     return JACOBI_OK;
 }
 
@@ -656,23 +792,22 @@ static int check_b_mode(jacobi_handle_t *h) {
 }
 
 // One time step with the device-side loop: one graph launch, one sync.
-static long long solve_step_device(jacobi_handle_t *h) {
-    TBJ_CUDA(h, cudaGraphLaunch(h->step, h->stream));
-    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
-    const LoopState st = *h->loop_host;
-    // Launches run (no-ops after the stop included): one body of
-    // intervals_per_iteration() intervals per iteration.
-    const long long checks = st.result_k / h->interval + 1;
+// Kernels one device-side step ran: reset + bmax, then per loop iteration
+// the body (no-op launches after the stop included) and its condition
+// kernel. A skipped step runs one iteration of no-ops.
+static long long device_step_launches(const jacobi_handle_t *h,
+                                      const LoopState &st) {
     const long long per_body = intervals_per_iteration(h->launches_per_check);
+    const long long checks =
+        st.status == kStepSkipped ? 1 : st.result_k / h->interval + 1;
     const long long iters = (checks + per_body - 1) / per_body;
-    // reset + bmax, then per iteration the body and its condition kernel
-    h->launches += 2 + iters * (per_body * h->launches_per_check + 1);
+    return 2 + iters * (per_body * h->launches_per_check + 1);
+}
+
+// Outcome of a device-side step from its final state: sweeps or a status.
+static long long device_step_outcome(jacobi_handle_t *h, const LoopState &st) {
     if (!st.stop)
         return fail(h, JACOBI_ERR_CUDA, "device loop ended without a decision");
-    h->cur = st.where;
-    int rc = settle(h);
-    if (rc) return rc;
-    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
     if (st.err & ERR_TMA_TIMEOUT)
         return fail(h, JACOBI_ERR_CUDA,
                     "a TMA load did not complete within its wait limit");
@@ -691,6 +826,51 @@ static long long solve_step_device(jacobi_handle_t *h) {
         default:
             return fail(h, JACOBI_ERR_CUDA, "device loop failed (%d)", st.status);
     }
+}
+
+static long long solve_step_device(jacobi_handle_t *h) {
+    TBJ_CUDA(h, cudaGraphLaunch(h->step, h->stream));
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    const LoopState st = *h->loop_host;
+    h->launches += device_step_launches(h, st);
+    if (st.stop) {
+        h->cur = st.where;
+        int rc = settle(h);
+        if (rc) return rc;
+        TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    }
+    return device_step_outcome(h, st);
+}
+
+// A whole run under device control: one graph launch, one synchronisation.
+static long long run_device(jacobi_handle_t *h, const float *g, int steps,
+                            long long *sweeps_per_step) {
+    int rc = settle(h);
+    if (rc) return rc;
+    if (!h->run || h->run_g != g || h->run_steps != steps)
+        if ((rc = record_run(h, g, steps))) return rc;
+    TBJ_CUDA(h, cudaGraphLaunch(h->run, h->stream));
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    h->b_mode = h->cfg.rhs;
+    const bool settle_needed = h->launches_per_check % 2 == 1;
+    long long total = 0;
+    for (int s = 0; s < steps; ++s) {
+        const LoopState st = h->run_states_host[s];
+        // right-hand side (two copies for the first unfused step)
+        h->launches += (h->cfg.rhs == JACOBI_RHS_UNFUSED && s == 0) ? 2 : 1;
+        h->launches += device_step_launches(h, st) + (settle_needed ? 1 : 0);
+        const long long k = device_step_outcome(h, st);
+        if (sweeps_per_step) sweeps_per_step[s] = k;
+        if (k < 0) {
+            // later steps were skipped on the device: count their kernels
+            for (int q = s + 1; q < steps; ++q)
+                h->launches += 1 + device_step_launches(h, h->run_states_host[q]) +
+                               (settle_needed ? 1 : 0);
+            return k;
+        }
+        total += k;
+    }
+    return total;
 }
 
 // Stopping rule at a check (section 01), shared by the host-driven loops:
@@ -856,6 +1036,13 @@ long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
                      long long *sweeps_per_step) {
     if (!h) return JACOBI_ERR_INVALID_ARG;
     if (steps < 0) return fail(h, JACOBI_ERR_INVALID_ARG, "steps must be >= 0");
+    if (steps > 0 && h->cfg.control == JACOBI_CONTROL_DEVICE && h->nlevels == 0) {
+        if (!g || !aligned16(g))
+            return fail(h, JACOBI_ERR_INVALID_ARG,
+                        "g must be a 16-byte aligned buffer");
+        h->trace.clear();
+        return run_device(h, g, steps, sweeps_per_step);
+    }
     long long total = 0;
     for (int s = 0; s < steps; ++s) {
         int rc = jacobi_rhs(h, g);
@@ -890,6 +1077,8 @@ void jacobi_destroy(jacobi_handle_t *h) {
     if (h->stream || h->capture) cudaStreamSynchronize(h->stream);
     destroy_graphs(h);
     destroy_levels(h);
+    if (h->run_states) cudaFree(h->run_states);
+    if (h->run_states_host) cudaFreeHost(h->run_states_host);
     for (auto &e : h->ev)
         if (e) cudaEventDestroy(e);
     if (h->capture) cudaStreamDestroy(h->capture);

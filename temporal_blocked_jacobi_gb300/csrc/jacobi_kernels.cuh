@@ -277,7 +277,14 @@ cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
                               const float *b, float *out,
                               const LaunchCtl &ctl, cudaStream_t stream);
 int sweep_sync_blocks(const GridDesc &g);
-cudaError_t launch_loop_reset(LoopState *st, cudaStream_t stream);
+// Status of a step that a multi-step graph skipped because an earlier step
+// failed (never returned to callers).
+constexpr int kStepSkipped = -100;
+cudaError_t launch_loop_reset(LoopState *st, const LoopState *prev,
+                              cudaStream_t stream);
+// If st->where == 1, copy the interior of src (u_alt) into dst (u).
+cudaError_t launch_settle(const GridDesc &g, const LoopState *st,
+                          const float *src, float *dst, cudaStream_t stream);
 // End of a loop iteration: clear the loop condition once LoopState::stop is
 // set. The sweep kernels only set the flag; keeping the graph call in this
 // one small kernel keeps it out of the sweep kernels.

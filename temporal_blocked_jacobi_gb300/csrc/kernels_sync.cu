@@ -318,7 +318,11 @@ __global__ void k_copy_interior(const float *__restrict__ src,
     }
 }
 
-__global__ void k_loop_reset(LoopState *st) {
+// Reset a step's loop state. In a graph of several time steps `prev` is the
+// previous step's state: if that step did not converge, this step is marked
+// skipped (stopped before it starts), so every later kernel of it returns at
+// entry.
+__global__ void k_loop_reset(LoopState *st, const LoopState *prev) {
     st->rmax = 0.f;
     st->bmax = 0.f;
     st->err = 0u;
@@ -329,6 +333,25 @@ __global__ void k_loop_reset(LoopState *st) {
     st->status = 0;
     st->where = 0;
     st->rbits = 0u;
+    if (prev && prev->status != 0) {
+        st->status = kStepSkipped;
+        st->stop = 1;
+    }
+}
+
+// End of a time step in a multi-step graph: if the answer sits in u_alt
+// (LoopState::where), copy its interior into u, so that the next step's
+// right-hand side and sweeps start from u.
+__global__ void k_settle(const LoopState *st, const float *__restrict__ src,
+                         float *__restrict__ dst, int n, long long ld) {
+    if (st->where != 1) return;  // same value for every thread
+    const int x0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (x0 >= n) return;
+    for (int i = 1 + blockIdx.y * blockDim.y + threadIdx.y; i <= n - 2;
+         i += gridDim.y * blockDim.y) {
+        const long long row = (long long)i * ld;
+        store_interior(dst + row, x0, n, ld4(src + row + x0));
+    }
 }
 
 // The loop condition starts at 1 with every launch of the step's graph, so
@@ -403,8 +426,16 @@ int sweep_sync_blocks(const GridDesc &g) {
     return (int)(grid.x * grid.y);
 }
 
-cudaError_t launch_loop_reset(LoopState *st, cudaStream_t stream) {
-    k_loop_reset<<<1, 1, 0, stream>>>(st);
+cudaError_t launch_loop_reset(LoopState *st, const LoopState *prev,
+                              cudaStream_t stream) {
+    k_loop_reset<<<1, 1, 0, stream>>>(st, prev);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_settle(const GridDesc &g, const LoopState *st,
+                          const float *src, float *dst, cudaStream_t stream) {
+    k_settle<<<elementwise_grid(g.n), dim3(32, 8), 0, stream>>>(st, src, dst,
+                                                                g.n, g.ld);
     return cudaGetLastError();
 }
 

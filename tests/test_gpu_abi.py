@@ -123,6 +123,77 @@ def test_sweep_cap_not_converged_then_recovers(control, strategy, depth):
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("strategy,depth", [("sync", 1), ("etb", 4), ("etb", 8), ("ba", 8)])
+def test_device_run_stops_at_failing_step(strategy, depth):
+    """jacobi_run under device control is one graph for all steps. With a
+    source so large that step 2's right-hand side overflows, step 1
+    converges and step 2 reports JACOBI_ERR_NONFINITE with u holding its last
+    checked iterate, as the oracle's run leaves it; later steps do nothing
+    and the handle works afterwards."""
+    import ctypes
+    import torch
+    import oracle
+    jacobi = _jacobi()
+    n, r = 40, 1.0
+    u0 = P.initial_field(n)
+    g = P.source_term(n, kind="zero")
+    g[20, 20] = np.float32(2e38)
+    ref = u0.copy()
+    ref_k = []
+    for _ in range(4):
+        bb = oracle.rhs(ref, g)
+        k, _, _ = oracle.solve_step(ref, bb, r, depth=depth if strategy == "ba" else 0)
+        ref_k.append(k)
+        if k < 0:
+            break
+    assert ref_k[0] > 0 and ref_k[1] == jacobi.ERR_NONFINITE
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    g_dev = to_dev(g)
+    with jacobi.Solver(u, u_alt, b, r, strategy=strategy, depth=depth,
+                       control="device") as s:
+        counts = (ctypes.c_longlong * 4)()
+        total = jacobi.load().jacobi_run(s.handle, ctypes.c_void_p(g_dev.data_ptr()),
+                                         4, counts)
+        assert total == jacobi.ERR_NONFINITE
+        assert [counts[0], counts[1]] == ref_k
+        assert "not finite" in s.last_error
+        torch.cuda.synchronize()
+        got = u.cpu().numpy()
+        # Non-finite at the same cells, every finite cell bit for bit. (Which
+        # non-finite value a cell holds may differ: the verified fixed-divisor
+        # division is IEEE-exact for finite numerators but turns an infinite
+        # one into NaN; NaN payloads differ between GPU and host too.)
+        bad = ~np.isfinite(ref)
+        assert bad.any()
+        assert np.array_equal(~np.isfinite(got), bad)
+        assert np.array_equal(got.view(np.uint32)[~bad], ref.view(np.uint32)[~bad])
+        u.copy_(to_dev(u0))
+        assert sum(s.run(to_dev(P.source_term(n, kind="gauss")), 2)) > 0
+
+
+def test_device_run_graph_follows_source_and_step_count():
+    """The run graph is rebuilt when the source buffer or the number of steps
+    changes; each run matches the oracle."""
+    import torch
+    import oracle
+    jacobi = _jacobi()
+    n, r = 70, 10.0
+    u0, g = workload(n, "gauss")
+    g2 = (g * np.float32(0.5)).astype(np.float32)
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    u.copy_(to_dev(u0))
+    ref = u0.copy()
+    with jacobi.Solver(u, u_alt, b, r, strategy="etb", depth=8,
+                       control="device") as s:
+        for src, steps in ((g, 3), (g2, 3), (g2, 2), (g, 1)):
+            got_k = s.run(to_dev(src), steps)
+            ref, ref_k, _ = oracle.run(ref, src, r, steps=steps, m=8)
+            assert got_k == ref_k
+        torch.cuda.synchronize()
+        assert np.array_equal(u.cpu().numpy(), ref)
+
+
 def test_nan_source_reports_nonfinite():
     jacobi = _jacobi()
     n = 64
