@@ -307,13 +307,16 @@ int record_batch(jacobi_handle_t *h, int start, cudaGraphExec_t *exec) {
     return JACOBI_OK;
 }
 
-// Check intervals per iteration of the device-side loop. Evaluating the
-// loop condition costs about as much as a launch, so an iteration runs about
-// eight launches' worth of intervals (launches after the stop return at
-// entry, so a few are wasted per time step). Even when an interval has an
-// odd number of launches, so that the body still ends in u.
-long long intervals_per_iteration(long long launches_per_check) {
-    const long long k = launches_per_check >= 8 ? 1 : 8 / launches_per_check;
+// Check intervals per iteration of the device-side loop. A loop iteration
+// costs a few launches' worth of time, so an iteration runs about `target`
+// launches (those after the stop return at entry, so some are wasted per
+// time step): 16 from N = 1024 on, where launches are long enough for the
+// saved iterations to win, 8 below (measured on GB300). Even when an
+// interval has an odd number of launches, so that the body ends in u.
+long long intervals_per_iteration(long long launches_per_check, int n) {
+    const long long target = n >= 1024 ? 16 : 8;
+    const long long k =
+        launches_per_check >= target ? 1 : target / launches_per_check;
     return (launches_per_check % 2 == 1 && k % 2 == 1) ? k + 1 : k;
 }
 
@@ -324,7 +327,7 @@ long long intervals_per_iteration(long long launches_per_check) {
 cudaError_t capture_body(jacobi_handle_t *h, LoopState *st,
                          cudaGraphConditionalHandle cond) {
     const long long L = h->launches_per_check;
-    const long long halves = intervals_per_iteration(L);
+    const long long halves = intervals_per_iteration(L, h->g.n);
     int src = 0;
     cudaError_t e = cudaSuccess;
     for (long long half = 0; half < halves && e == cudaSuccess; ++half)
@@ -797,7 +800,7 @@ static int check_b_mode(jacobi_handle_t *h) {
 // kernel. A skipped step runs one iteration of no-ops.
 static long long device_step_launches(const jacobi_handle_t *h,
                                       const LoopState &st) {
-    const long long per_body = intervals_per_iteration(h->launches_per_check);
+    const long long per_body = intervals_per_iteration(h->launches_per_check, h->g.n);
     const long long checks =
         st.status == kStepSkipped ? 1 : st.result_k / h->interval + 1;
     const long long iters = (checks + per_body - 1) / per_body;
