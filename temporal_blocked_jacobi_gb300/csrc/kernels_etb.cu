@@ -154,6 +154,87 @@ __device__ __forceinline__ float4 hold4(float4 nv, float4 old, bool row_ok,
     return o;
 }
 
+// One sweep of one tile. RESID: also reduce |J(u) - u| (first sweep of a
+// fused launch); LAST: write the tile to global memory instead of to dst.
+template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool RESID,
+          bool LAST>
+__device__ __forceinline__ void etb_sweep(const float *src, float *dst, int s,
+                                          const float4 (&breg)[RW][CH],
+                                          float *__restrict__ out, int n,
+                                          long long ld, float r, float d,
+                                          float y, int bxo, int byo,
+                                          const unsigned (&colmask)[CH],
+                                          const bool (&in_tile)[CH],
+                                          unsigned &rm) {
+    using S = EtbShape<D, CH, RW, NW>;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int band = warp * RW;
+    const int col = 4 * lane;
+    const int left = (lane + 31) & 31, right = (lane + 1) & 31;
+    if (!(band + RW > s + 1 && band < S::BY - 1 - s)) return;
+    const float *sp = src + band * S::BX + col;
+    float *dp = dst + band * S::BX + col;
+    float4 nr[CH], cr[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        nr[c] = lds4(sp - S::BX + 128 * c);
+        cr[c] = lds4(sp + 128 * c);
+    }
+#pragma unroll
+    for (int j = 0; j < RW; ++j) {
+        float4 sr[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) sr[c] = lds4(sp + (j + 1) * S::BX + 128 * c);
+        float wv[CH], ev[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            wv[c] = __shfl_sync(FULL, cr[c].w, left);
+            ev[c] = __shfl_sync(FULL, cr[c].x, right);
+        }
+        const int row = band + j;
+        const int gy = byo + row;
+        const bool row_ok = !EDGE || (gy >= 1 && gy <= n - 2);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
+            const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
+            float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w, e, r,
+                                      d, y);
+            if (RESID) {
+                const bool tile_row = row >= D && row < D + S::TY;
+                if (in_tile[c] && tile_row && row_ok) {
+                    const float4 c4 = cr[c];
+                    const unsigned m = colmask[c];
+                    if (m & 1u) rm = max(rm, change_bits(nv.x, c4.x));
+                    if (m & 2u) rm = max(rm, change_bits(nv.y, c4.y));
+                    if (m & 4u) rm = max(rm, change_bits(nv.z, c4.z));
+                    if (m & 8u) rm = max(rm, change_bits(nv.w, c4.w));
+                }
+            }
+            if (EDGE) nv = hold4(nv, cr[c], row_ok, colmask[c]);
+            if (!LAST) {
+                sts4(dp + j * S::BX + 128 * c, nv);
+            } else {
+                const bool tile_row = row >= D && row < D + S::TY;
+                if (in_tile[c] && tile_row && row_ok) {
+                    float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
+                    if (colmask[c] == 0xfu) {
+                        sts4(g, nv);
+                    } else {
+                        if (colmask[c] & 1u) g[0] = nv.x;
+                        if (colmask[c] & 2u) g[1] = nv.y;
+                        if (colmask[c] & 4u) g[2] = nv.z;
+                        if (colmask[c] & 8u) g[3] = nv.w;
+                    }
+                }
+            }
+            nr[c] = cr[c];
+            cr[c] = sr[c];
+        }
+    }
+}
+
 // D sweeps of one tile. sA, sB point at box row 0 of the two buffers (rows
 // -1 and BY exist); b of this warp's band is in breg.
 template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool FUSED>
@@ -164,13 +245,7 @@ __device__ __forceinline__ void etb_sweeps(float *sA, float *sB,
                                            float y, int bxo, int byo,
                                            unsigned &rm) {
     using S = EtbShape<D, CH, RW, NW>;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int band = warp * RW;
-    const int col = 4 * lane;  // this lane's column within a 128-wide chunk
-    const int left = (lane + 31) & 31, right = (lane + 1) & 31;
-
-    // Columns of this lane's chunks that are interior grid cells (edge tiles).
+    const int col = 4 * (threadIdx.x & 31);
     unsigned colmask[CH];
     bool in_tile[CH];
 #pragma unroll
@@ -185,75 +260,24 @@ __device__ __forceinline__ void etb_sweeps(float *sA, float *sB,
         colmask[c] = EDGE ? m : 0xfu;
         in_tile[c] = bx >= S::HX && bx < S::HX + S::TX;
     }
-
+    // Sweep 0 (with the residual in a fused launch), sweeps 1 .. D-2, and
+    // the last sweep, which writes the tile out.
+    etb_sweep<D, CH, RW, NW, FAST, EDGE, FUSED, false>(
+        sA, sB, 0, breg, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rm);
+    __syncthreads();
 #pragma unroll 1
-    for (int s = 0; s < D; ++s) {
+    for (int s = 1; s < D - 1; ++s) {
         const float *src = (s & 1) ? sB : sA;
         float *dst = (s & 1) ? sA : sB;
-        const bool last = (s == D - 1);
-        // Skip the band if none of its rows is still needed.
-        if (band + RW > s + 1 && band < S::BY - 1 - s) {
-            const float *sp = src + band * S::BX + col;
-            float *dp = dst + band * S::BX + col;
-            float4 nr[CH], cr[CH];
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                nr[c] = lds4(sp - S::BX + 128 * c);
-                cr[c] = lds4(sp + 128 * c);
-            }
-#pragma unroll
-            for (int j = 0; j < RW; ++j) {
-                float4 sr[CH];
-#pragma unroll
-                for (int c = 0; c < CH; ++c)
-                    sr[c] = lds4(sp + (j + 1) * S::BX + 128 * c);
-                float wv[CH], ev[CH];
-#pragma unroll
-                for (int c = 0; c < CH; ++c) {
-                    wv[c] = __shfl_sync(FULL, cr[c].w, left);
-                    ev[c] = __shfl_sync(FULL, cr[c].x, right);
-                }
-                const int row = band + j;
-                const int gy = byo + row;
-                const bool row_ok = !EDGE || (gy >= 1 && gy <= n - 2);
-                const bool tile_row = row >= D && row < D + S::TY;
-#pragma unroll
-                for (int c = 0; c < CH; ++c) {
-                    const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
-                    const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
-                    float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w,
-                                              e, r, d, y);
-                    if (FUSED && s == 0 && in_tile[c] && tile_row && row_ok) {
-                        // |J(u) - u| of the launch's input at the tile's
-                        // interior cells.
-                        const float4 c4 = cr[c];
-                        const unsigned m = colmask[c];
-                        if (m & 1u) rm = max(rm, change_bits(nv.x, c4.x));
-                        if (m & 2u) rm = max(rm, change_bits(nv.y, c4.y));
-                        if (m & 4u) rm = max(rm, change_bits(nv.z, c4.z));
-                        if (m & 8u) rm = max(rm, change_bits(nv.w, c4.w));
-                    }
-                    if (EDGE) nv = hold4(nv, cr[c], row_ok, colmask[c]);
-                    if (!last) {
-                        sts4(dp + j * S::BX + 128 * c, nv);
-                    } else if (in_tile[c] && tile_row && row_ok) {
-                        float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
-                        if (colmask[c] == 0xfu) {
-                            sts4(g, nv);
-                        } else {
-                            if (colmask[c] & 1u) g[0] = nv.x;
-                            if (colmask[c] & 2u) g[1] = nv.y;
-                            if (colmask[c] & 4u) g[2] = nv.z;
-                            if (colmask[c] & 8u) g[3] = nv.w;
-                        }
-                    }
-                    nr[c] = cr[c];
-                    cr[c] = sr[c];
-                }
-            }
-        }
-        if (!last) __syncthreads();
+        etb_sweep<D, CH, RW, NW, FAST, EDGE, false, false>(
+            src, dst, s, breg, out, n, ld, r, d, y, bxo, byo, colmask, in_tile,
+            rm);
+        __syncthreads();
     }
+    // D is even: the last sweep reads sB.
+    etb_sweep<D, CH, RW, NW, FAST, EDGE, false, true>(
+        sB, sA, D - 1, breg, out, n, ld, r, d, y, bxo, byo, colmask, in_tile,
+        rm);
 }
 
 // Issue the TMA loads of one tile's box of u (into a) and of b (into bb).
