@@ -383,7 +383,11 @@ def kernel_name(tok):
     if kw["strategy"] == "sync":
         return "k_sweep_sync" + (" (unfused rhs)" if kw.get("rhs") == "unfused" else "")
     if kw["strategy"] == "etb":
-        return f"k_etb (D={kw['depth']})"
+        # default shapes: bands in registers for D = 4, 8 and 16, box in
+        # shared memory for D = 2
+        name = ("k_etbr" if kw["depth"] in (4, 8, 16) and kw.get("tile", (0, 0)) == (0, 0)
+                else "k_etb")
+        return f"{name} (D={kw['depth']})"
     return f"k_ba / k_block_async (D={kw['depth']})"
 
 

@@ -11,11 +11,14 @@
 // boundary), the top/bottom halo D rows, so the tile is
 // TX = BX - 2*HX by TY = BY - 2*D cells.
 //
-// The block is persistent: it walks tiles k, k + gridDim.x, ... Thread 0
-// loads a tile's box of u and of b with two TMA copies onto an mbarrier
-// (bounded wait); with NB = 2 buffer sets the next tile is loaded while the
-// current one is swept, with NB = 1 right after it. Each warp keeps its
-// band's b in registers; the field ping-pongs between two shared buffers,
+// Two kernels share this layout. Both are persistent: a block walks tiles
+// k, k + gridDim.x, ... and thread 0 loads a tile's box of u and of b with
+// two TMA copies onto an mbarrier (bounded wait).
+//
+// k_etb (box in shared memory): with NB = 2 buffer sets the next tile is
+// loaded while the current one is swept, with NB = 1 right after it. Each
+// warp keeps its band's b in registers; the field ping-pongs between two
+// shared buffers,
 // each with a spare row above and below the box so that every row of every
 // band can be updated without a bounds test. In sweep s each warp updates
 // its whole band over the full box width -- bands lying entirely outside the
@@ -26,6 +29,11 @@
 // D sweeps the tile (HX >= D columns and D rows in from the edge) holds
 // exactly the result of D synchronous sweeps. The last sweep writes the tile
 // to global memory.
+//
+// k_etbr (bands in registers) keeps the same band decomposition, skipping and
+// inward-moving exactness, but each warp holds its RW rows in registers for
+// all D sweeps and trades only its top and bottom rows through shared memory
+// (see the comment above k_etbr).
 //
 // With the verified fixed-divisor division the update of a lane's four
 // cells uses packed float32 pairs for everything but the west+east sums.
@@ -300,8 +308,9 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map_src,
 // over a tiles_x-wide tile grid). With NB = 2 the TMA engine fills the other
 // buffer set with the next tile while the block sweeps the current one; with
 // NB = 1 the next tile's load is issued as soon as the current tile is done.
-template <int D, int CH, int RW, int NW, int NB, bool FAST, bool FUSED>
-__global__ void __launch_bounds__(32 * NW, 1)
+template <int D, int CH, int RW, int NW, int NB, int MINB, bool FAST,
+          bool FUSED>
+__global__ void __launch_bounds__(32 * NW, MINB)
 k_etb(const __grid_constant__ CUtensorMap map_src,
       const __grid_constant__ CUtensorMap map_b, float *__restrict__ out,
       int n, long long ld, float r, float d, float y, unsigned *err,
@@ -404,47 +413,342 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
     if (FUSED) fused_block_finish(rm, lp, fin_scratch);
 }
 
-// Shapes per depth: {CH, RW, NW, NB}. The first one of a depth is its
-// default (fastest measured on GB300).
-struct EtbVariant {
-    int depth, ch, rw, nw, nb;
-};
-constexpr EtbVariant kVariants[] = {
-    {2, 1, 3, 32, 2}, {2, 1, 4, 16, 2}, {2, 2, 4, 16, 1},
-    {4, 1, 3, 32, 2}, {4, 1, 4, 16, 2}, {4, 2, 4, 16, 1},
-    {8, 1, 3, 32, 2}, {8, 1, 4, 16, 2}, {8, 1, 4, 32, 1}, {8, 2, 4, 16, 1},
-    {16, 1, 4, 32, 1}, {16, 1, 3, 32, 2}, {16, 2, 3, 32, 1},
+// ---------------------------------------------------------------------------
+// Register-resident bands. The same exact temporal blocking, but a warp keeps
+// the RW rows of its band in registers for all D sweeps of a tile instead of
+// ping-ponging the whole box through shared memory. Shared memory holds the
+// TMA staging boxes of u and b (read once per tile) and, per sweep parity,
+// the top and bottom row of every band: after each sweep a warp publishes
+// its two edge rows and, past the barrier, reads the row above and the row
+// below its band from its neighbours' entries. Per band and sweep that is
+// two shared loads and two shared stores instead of 2 + 2*RW, and the
+// staging boxes are free for the next tile's TMA load from the first sweep
+// on. Slots -1 and 2*NW of the exchange rows (above the first band, below
+// the last) stay zero; the cells that read them lie outside the region that
+// is still exact.
+// ---------------------------------------------------------------------------
+template <int D, int CH, int RW, int NW>
+struct EtbrShape {
+    static constexpr int BX = 128 * CH;
+    static constexpr int BY = NW * RW;
+    static constexpr int HX = (D + 3) / 4 * 4;
+    static constexpr int TX = BX - 2 * HX;
+    static constexpr int TY = BY - 2 * D;
+    static constexpr size_t BOX_BYTES = (size_t)BX * BY * sizeof(float);
+    static constexpr int XROWS = 2 * NW + 2;  // exchange slots -1 .. 2*NW
+    static constexpr size_t SMEM =
+        256 + 2 * BOX_BYTES + 2 * (size_t)XROWS * BX * sizeof(float);
+    static_assert(TX >= 4 && TY >= 1, "tile too small for this depth");
+    static_assert(BX <= 256 && BY <= 256, "TMA box dimension limit");
+    static_assert(SMEM <= 227 * 1024, "shared memory per block");
 };
 
-template <int D, int CH, int RW, int NW, int NB>
+// One sweep of a band held in registers. hn / hs: the row above / below the
+// band (input state of this sweep). RESID and LAST as in etb_sweep.
+template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool RESID,
+          bool LAST>
+__device__ __forceinline__ void etbr_band(float4 (&u)[RW][CH],
+                                          const float4 (&b)[RW][CH],
+                                          const float4 (&hn)[CH],
+                                          const float4 (&hs)[CH],
+                                          float *__restrict__ out, int n,
+                                          long long ld, float r, float d,
+                                          float y, int bxo, int byo,
+                                          const unsigned (&colmask)[CH],
+                                          const bool (&in_tile)[CH],
+                                          unsigned &rm) {
+    using S = EtbrShape<D, CH, RW, NW>;
+    const int lane = threadIdx.x & 31;
+    const int band = (threadIdx.x >> 5) * RW;
+    const int col = 4 * lane;
+    const int left = (lane + 31) & 31, right = (lane + 1) & 31;
+    float4 prev[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) prev[c] = hn[c];
+#pragma unroll
+    for (int j = 0; j < RW; ++j) {
+        float wv[CH], ev[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            wv[c] = __shfl_sync(FULL, u[j][c].w, left);
+            ev[c] = __shfl_sync(FULL, u[j][c].x, right);
+        }
+        const int row = band + j;
+        const int gy = byo + row;
+        const bool row_ok = !EDGE || (gy >= 1 && gy <= n - 2);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
+            const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
+            const float4 cur = u[j][c];
+            const float4 nxt = (j + 1 < RW) ? u[j + 1 < RW ? j + 1 : j][c] : hs[c];
+            float4 nv = update4<FAST>(prev[c], cur, nxt, b[j][c], w, e, r, d, y);
+            if (RESID) {
+                const bool tile_row = row >= D && row < D + S::TY;
+                if (in_tile[c] && tile_row && row_ok) {
+                    const unsigned m = colmask[c];
+                    if (m & 1u) rm = max(rm, change_bits(nv.x, cur.x));
+                    if (m & 2u) rm = max(rm, change_bits(nv.y, cur.y));
+                    if (m & 4u) rm = max(rm, change_bits(nv.z, cur.z));
+                    if (m & 8u) rm = max(rm, change_bits(nv.w, cur.w));
+                }
+            }
+            if (EDGE) nv = hold4(nv, cur, row_ok, colmask[c]);
+            if (LAST) {
+                const bool tile_row = row >= D && row < D + S::TY;
+                if (in_tile[c] && tile_row && row_ok) {
+                    float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
+                    if (colmask[c] == 0xfu) {
+                        sts4(g, nv);
+                    } else {
+                        if (colmask[c] & 1u) g[0] = nv.x;
+                        if (colmask[c] & 2u) g[1] = nv.y;
+                        if (colmask[c] & 4u) g[2] = nv.z;
+                        if (colmask[c] & 8u) g[3] = nv.w;
+                    }
+                }
+            }
+            prev[c] = cur;
+            u[j][c] = nv;
+        }
+    }
+}
+
+// D sweeps of one tile with register-resident bands. xb: the exchange rows
+// (two parities of XROWS rows of BX floats; slot k of parity q at row
+// q * XROWS + k + 1). On entry u, b, hn, hs hold the tile's input.
+template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool FUSED>
+__device__ __forceinline__ void etbr_sweeps(float4 (&u)[RW][CH],
+                                            const float4 (&b)[RW][CH],
+                                            float4 (&hn)[CH], float4 (&hs)[CH],
+                                            float *xb, float *__restrict__ out,
+                                            int n, long long ld, float r,
+                                            float d, float y, int bxo, int byo,
+                                            unsigned &rm) {
+    using S = EtbrShape<D, CH, RW, NW>;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int band = warp * RW;
+    const int col = 4 * lane;
+    unsigned colmask[CH];
+    bool in_tile[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int bx = 128 * c + col;
+        unsigned m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int gx = bxo + bx + k;
+            m |= (gx >= 1 && gx <= n - 2) ? (1u << k) : 0u;
+        }
+        colmask[c] = EDGE ? m : 0xfu;
+        in_tile[c] = bx >= S::HX && bx < S::HX + S::TX;
+    }
+    // This band's own slots (2*warp: top row, 2*warp + 1: bottom row) and
+    // those of the rows next to it, at parity 0; parity 1 is XROWS rows on.
+    float *own = xb + (2 * warp + 1) * S::BX + col;
+    const float *above = xb + (2 * warp) * S::BX + col;      // slot 2w - 1
+    const float *below = xb + (2 * warp + 3) * S::BX + col;  // slot 2w + 2
+    constexpr int PAR = S::XROWS * S::BX;
+
+    // Publish the band's edge rows into parity q and, past the barrier, read
+    // the rows next to the band for sweep s + 1.
+    auto exchange = [&](int s) {
+        const int q = (s + 1) & 1;
+        if (band + RW > s + 1 && band < S::BY - 1 - s) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                sts4(own + q * PAR + 128 * c, u[0][c]);
+                sts4(own + q * PAR + S::BX + 128 * c, u[RW - 1][c]);
+            }
+        }
+        __syncthreads();
+        if (band + RW > s + 2 && band < S::BY - 2 - s) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                hn[c] = lds4(above + q * PAR + 128 * c);
+                hs[c] = lds4(below + q * PAR + 128 * c);
+            }
+        }
+    };
+
+    if (band + RW > 1 && band < S::BY - 1)
+        etbr_band<D, CH, RW, NW, FAST, EDGE, FUSED, false>(
+            u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rm);
+    exchange(0);
+#pragma unroll 1
+    for (int s = 1; s < D - 1; ++s) {
+        if (band + RW > s + 1 && band < S::BY - 1 - s)
+            etbr_band<D, CH, RW, NW, FAST, EDGE, false, false>(
+                u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile,
+                rm);
+        exchange(s);
+    }
+    if (band + RW > D && band < S::BY - D)
+        etbr_band<D, CH, RW, NW, FAST, EDGE, false, true>(
+            u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rm);
+}
+
+// Persistent kernel with register-resident bands: block k handles tiles k,
+// k + gridDim.x, ... One staging set: the next tile's boxes are loaded as
+// soon as every warp has taken the current tile into registers.
+template <int D, int CH, int RW, int NW, int MINB, bool FAST, bool FUSED>
+__global__ void __launch_bounds__(32 * NW, MINB)
+k_etbr(const __grid_constant__ CUtensorMap map_src,
+       const __grid_constant__ CUtensorMap map_b, float *__restrict__ out,
+       int n, long long ld, float r, float d, float y, unsigned *err,
+       const int *stop, LoopParams lp, int tiles_x, int tiles) {
+    using S = EtbrShape<D, CH, RW, NW>;
+    using L = EtbShape<D, CH, RW, NW, 1>;  // tile geometry for load_tile
+    __shared__ unsigned fin_scratch[33];
+    allow_dependents();
+
+    // [barrier | u box | b box | exchange rows], box rows 512 or 1024 bytes.
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + pad);
+    float *su = reinterpret_cast<float *>(smem_raw + pad + 128);
+    float *sb = su + S::BX * S::BY;
+    float *xb = sb + S::BX * S::BY;
+
+    const int tid = threadIdx.x;
+    for (int k = tid; k < S::BX; k += 32 * NW)
+        for (int q = 0; q < 2; ++q) {
+            xb[q * S::XROWS * S::BX + k] = 0.f;  // slot -1
+            xb[(q * S::XROWS + S::XROWS - 1) * S::BX + k] = 0.f;  // slot 2 NW
+        }
+    if (tid == 0) {
+        mbar_init(bar);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    grid_dependency_wait();
+    if (stop && *stop) return;  // same value for every thread of the launch
+    if (tid == 0 && (int)blockIdx.x < tiles)
+        load_tile<L>(&map_src, &map_b, bar, su, sb, blockIdx.x, tiles_x, D);
+    __syncthreads();
+
+    const int lane = tid & 31;
+    const int band = (tid >> 5) * RW;
+    unsigned rm = 0u;
+    bool failed = false;
+    unsigned fail_parity = 0u;
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+        const unsigned parity = (unsigned)i & 1u;
+        const bool ok = mbar_wait_parity(bar, parity);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            fail_parity = parity;
+            break;
+        }
+        float4 u[RW][CH], b[RW][CH], hn[CH], hs[CH];
+#pragma unroll
+        for (int j = 0; j < RW; ++j)
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                u[j][c] = lds4(su + (band + j) * S::BX + 128 * c + 4 * lane);
+                b[j][c] = lds4(sb + (band + j) * S::BX + 128 * c + 4 * lane);
+            }
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            hn[c] = band > 0 ? lds4(su + (band - 1) * S::BX + 128 * c + 4 * lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            hs[c] = band + RW < S::BY
+                        ? lds4(su + (band + RW) * S::BX + 128 * c + 4 * lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // The staging boxes are consumed: load the next tile into them.
+        __syncthreads();
+        if (tid == 0 && t + (int)gridDim.x < tiles) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            load_tile<L>(&map_src, &map_b, bar, su, sb, t + gridDim.x, tiles_x, D);
+        }
+        const int gx0 = (t % tiles_x) * S::TX, gy0 = (t / tiles_x) * S::TY;
+        const int bxo = gx0 - S::HX, byo = gy0 - D;
+        const bool edge = bxo < 1 || byo < 1 || bxo + S::BX > n - 1 ||
+                          byo + S::BY > n - 1;
+        if (edge)
+            etbr_sweeps<D, CH, RW, NW, FAST, true, FUSED>(
+                u, b, hn, hs, xb, out, n, ld, r, d, y, bxo, byo, rm);
+        else
+            etbr_sweeps<D, CH, RW, NW, FAST, false, FUSED>(
+                u, b, hn, hs, xb, out, n, ld, r, d, y, bxo, byo, rm);
+    }
+    if (failed) {
+        if (tid == 0) atomicOr(err, (unsigned)ERR_TMA_TIMEOUT);
+        // Only the load waited on can be in flight: give it one more bounded
+        // wait before shared memory is released.
+        mbar_wait_parity(bar, fail_parity);
+    }
+    if (FUSED) fused_block_finish(rm, lp, fin_scratch);
+}
+
+// Shapes per depth: {KIND, CH, RW, NW, NB}; KIND 0 ping-pongs the box
+// through shared memory (k_etb, NB buffer sets), KIND 1 keeps the bands in
+// registers (k_etbr, one staging set). The first shape of a depth is its
+// default (fastest measured on GB300); the others are selected by their exact
+// tile size, the first listed winning.
+struct EtbVariant {
+    int depth, kind, ch, rw, nw, nb, minb;
+};
+constexpr EtbVariant kVariants[] = {
+    {2, 0, 1, 3, 32, 2, 1}, {2, 0, 1, 4, 16, 2, 1}, {2, 0, 2, 4, 16, 1, 1},
+    {4, 1, 1, 6, 16, 1, 1}, {4, 0, 1, 4, 16, 2, 1}, {4, 0, 2, 4, 16, 1, 1},
+    {4, 1, 1, 3, 16, 1, 2},
+    {8, 1, 1, 6, 16, 1, 1}, {8, 0, 1, 4, 16, 2, 1}, {8, 0, 1, 4, 32, 1, 1},
+    {8, 0, 2, 4, 16, 1, 1},
+    {16, 1, 1, 6, 16, 1, 1}, {16, 0, 1, 4, 32, 1, 1}, {16, 0, 2, 3, 32, 1, 1},
+};
+
+template <int K, int D, int CH, int RW, int NW, int NB, int MB, bool F,
+          bool FU>
+constexpr auto etb_kernel() {
+    if constexpr (K == 0)
+        return k_etb<D, CH, RW, NW, NB, MB, F, FU>;
+    else
+        return k_etbr<D, CH, RW, NW, MB, F, FU>;
+}
+
+template <int K, int D, int CH, int RW, int NW, int NB>
+constexpr size_t etb_smem() {
+    if constexpr (K == 0)
+        return EtbShape<D, CH, RW, NW, NB>::SMEM;
+    else
+        return EtbrShape<D, CH, RW, NW>::SMEM;
+}
+
+template <int K, int D, int CH, int RW, int NW, int NB, int MB>
 cudaError_t launch_variant(const GridDesc &g, const TileConf &tc,
                            const CUtensorMap *map_src,
                            const CUtensorMap *map_b, float *out,
                            unsigned *err, const LaunchCtl &ctl,
                            cudaStream_t stream) {
     using S = EtbShape<D, CH, RW, NW, NB>;
+    constexpr size_t smem = etb_smem<K, D, CH, RW, NW, NB>();
     const int tiles_x = (g.n - 1 + S::TX - 1) / S::TX;
     const int tiles = tiles_x * ((g.n - 1 + S::TY - 1) / S::TY);
-#define TBJ_K(F, FU)                                                           \
-    launch_pdl(k_etb<D, CH, RW, NW, NB, F, FU>, dim3(tc.ctas), dim3(32 * NW),  \
-               S::SMEM, stream, *map_src, *map_b, out, g.n, g.ld, g.r, g.d,   \
-               g.y, err, ctl.stop, ctl.lp, tiles_x, tiles)
+#define TBJ_K(F, FU)                                                          \
+    launch_pdl(etb_kernel<K, D, CH, RW, NW, NB, MB, F, FU>(), dim3(tc.ctas),     \
+               dim3(32 * NW), smem, stream, *map_src, *map_b, out, g.n,      \
+               g.ld, g.r, g.d, g.y, err, ctl.stop, ctl.lp, tiles_x, tiles)
     if (g.fast) return ctl.fused ? TBJ_K(true, true) : TBJ_K(true, false);
     return ctl.fused ? TBJ_K(false, true) : TBJ_K(false, false);
 #undef TBJ_K
 }
 
-template <int D, int CH, int RW, int NW, int NB>
+template <int K, int D, int CH, int RW, int NW, int NB, int MB>
 cudaError_t prepare_variant(TileConf &tc, int n) {
     using S = EtbShape<D, CH, RW, NW, NB>;
+    constexpr size_t smem = etb_smem<K, D, CH, RW, NW, NB>();
+    static_assert(smem <= 227 * 1024, "shared memory per block");
     const void *kernels[4] = {
-        (const void *)k_etb<D, CH, RW, NW, NB, true, false>,
-        (const void *)k_etb<D, CH, RW, NW, NB, false, false>,
-        (const void *)k_etb<D, CH, RW, NW, NB, true, true>,
-        (const void *)k_etb<D, CH, RW, NW, NB, false, true>};
+        (const void *)etb_kernel<K, D, CH, RW, NW, NB, MB, true, false>(),
+        (const void *)etb_kernel<K, D, CH, RW, NW, NB, MB, false, false>(),
+        (const void *)etb_kernel<K, D, CH, RW, NW, NB, MB, true, true>(),
+        (const void *)etb_kernel<K, D, CH, RW, NW, NB, MB, false, true>()};
     for (const void *k : kernels) {
         cudaError_t e = cudaFuncSetAttribute(
-            k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+            k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     // Persistent grid: as many blocks as fit on the GPU at once, at most one
@@ -455,29 +759,32 @@ cudaError_t prepare_variant(TileConf &tc, int n) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, k_etb<D, CH, RW, NW, NB, true, false>, 32 * NW, S::SMEM);
+            &per_sm, etb_kernel<K, D, CH, RW, NW, NB, MB, true, false>(), 32 * NW,
+            smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int tiles = ((n - 1 + S::TX - 1) / S::TX) * ((n - 1 + S::TY - 1) / S::TY);
     tc.ctas = sms * per_sm < tiles ? sms * per_sm : tiles;
+    tc.smem = smem;
     return cudaSuccess;
 }
 
-// Dispatch on a variant index (into kVariants).
-#define TBJ_ETB_VARIANTS(X) \
-    X(0, 2, 1, 3, 32, 2)    \
-    X(1, 2, 1, 4, 16, 2)    \
-    X(2, 2, 2, 4, 16, 1)    \
-    X(3, 4, 1, 3, 32, 2)    \
-    X(4, 4, 1, 4, 16, 2)    \
-    X(5, 4, 2, 4, 16, 1)    \
-    X(6, 8, 1, 3, 32, 2)    \
-    X(7, 8, 1, 4, 16, 2)    \
-    X(8, 8, 1, 4, 32, 1)    \
-    X(9, 8, 2, 4, 16, 1)    \
-    X(10, 16, 1, 4, 32, 1)  \
-    X(11, 16, 1, 3, 32, 2)  \
-    X(12, 16, 2, 3, 32, 1)
+// Dispatch on a variant index (into kVariants): I, KIND, D, CH, RW, NW, NB, MINB.
+#define TBJ_ETB_VARIANTS(X)        \
+    X(0, 0, 2, 1, 3, 32, 2, 1)     \
+    X(1, 0, 2, 1, 4, 16, 2, 1)     \
+    X(2, 0, 2, 2, 4, 16, 1, 1)     \
+    X(3, 1, 4, 1, 6, 16, 1, 1)     \
+    X(4, 0, 4, 1, 4, 16, 2, 1)     \
+    X(5, 0, 4, 2, 4, 16, 1, 1)     \
+    X(6, 1, 4, 1, 3, 16, 1, 2)     \
+    X(7, 1, 8, 1, 6, 16, 1, 1)     \
+    X(8, 0, 8, 1, 4, 16, 2, 1)     \
+    X(9, 0, 8, 1, 4, 32, 1, 1)     \
+    X(10, 0, 8, 2, 4, 16, 1, 1)    \
+    X(11, 1, 16, 1, 6, 16, 1, 1)   \
+    X(12, 0, 16, 1, 4, 32, 1, 1)   \
+    X(13, 0, 16, 2, 3, 32, 1, 1)
 
 }  // namespace
 
@@ -507,7 +814,7 @@ int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->tile_y = tc->box_y - 2 * depth;
     tc->origin = 0;
     tc->threads = 32 * k.nw;
-    tc->smem = 256 + 2 * (size_t)k.nb * tc->box_x * (tc->box_y + 2) * sizeof(float);
+    tc->smem = 0;  // set by prepare_sweep_etb
     tc->variant = pick;
     tc->ctas = 0;  // set by prepare_sweep_etb
     tc->stream = tc->ch = tc->sx = tc->sy = tc->grid_x = tc->grid_y = 0;
@@ -516,9 +823,9 @@ int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
 
 cudaError_t prepare_sweep_etb(TileConf &tc, int n) {
     switch (tc.variant) {
-#define TBJ_PREP(I, D, CH, RW, NW, NB) \
-    case I:                            \
-        return prepare_variant<D, CH, RW, NW, NB>(tc, n);
+#define TBJ_PREP(I, K, D, CH, RW, NW, NB, MB) \
+    case I:                                   \
+        return prepare_variant<K, D, CH, RW, NW, NB, MB>(tc, n);
         TBJ_ETB_VARIANTS(TBJ_PREP)
 #undef TBJ_PREP
         default:
@@ -533,9 +840,9 @@ cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              cudaStream_t stream) {
     unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
     switch (tc.variant) {
-#define TBJ_LAUNCH(I, D, CH, RW, NW, NB) \
-    case I:                              \
-        return launch_variant<D, CH, RW, NW, NB>(g, tc, map_src, map_b, out, err, ctl, stream);
+#define TBJ_LAUNCH(I, K, D, CH, RW, NW, NB, MB) \
+    case I:                                     \
+        return launch_variant<K, D, CH, RW, NW, NB, MB>(g, tc, map_src, map_b, out, err, ctl, stream);
         TBJ_ETB_VARIANTS(TBJ_LAUNCH)
 #undef TBJ_LAUNCH
         default:

@@ -51,6 +51,26 @@ def test_n2048_r10_gauss_bit_exact(n2048_reference, strategy, depth, control):
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
 
 
+# Non-default compiled tile shapes of exact temporal blocking (the defaults
+# run in the N = 2048 test above).
+ETB_SHAPES = [(2, (120, 60)), (2, (248, 60)), (4, (120, 56)), (4, (248, 56)),
+              (4, (120, 40)), (8, (112, 48)), (8, (112, 112)), (8, (240, 48)),
+              (16, (96, 96)), (16, (224, 64))]
+
+
+@pytest.mark.parametrize("depth,tile", ETB_SHAPES)
+def test_etb_tile_shapes_device_loop_bit_exact(depth, tile):
+    """Every compiled tile shape through the device-side loop, whose first
+    launch per check interval also reduces the residual: same sweep counts and
+    field as the oracle on a grid of several tiles with ragged edges."""
+    u0, g = workload(300, "gauss")
+    ref_u, ref_k, _ = oracle.run(u0, g, 10.0, steps=2, m=max(8, depth))
+    got_u, got_k, _ = gpu_run(u0, g, 10.0, steps=2, strategy="etb", depth=depth,
+                              tile=tile, control="device")
+    assert got_k == ref_k
+    assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
+
+
 @pytest.mark.parametrize("control", CONTROLS)
 def test_n2048_r10_gauss_unfused_sync_bit_exact(n2048_reference, control):
     """The unfused right-hand side (section 05, Table VI) changes the
