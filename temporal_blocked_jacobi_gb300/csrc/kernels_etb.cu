@@ -427,6 +427,13 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
 // the last) stay zero; the cells that read them lie outside the region that
 // is still exact.
 // ---------------------------------------------------------------------------
+// max(a, |x|) that returns NaN when either is NaN.
+__device__ __forceinline__ float max_nan_abs(float a, float x) {
+    float o;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(o) : "f"(a), "f"(fabsf(x)));
+    return o;
+}
+
 template <int D, int CH, int RW, int NW>
 struct EtbrShape {
     static constexpr int BX = 128 * CH;
@@ -456,7 +463,7 @@ __device__ __forceinline__ void etbr_band(float4 (&u)[RW][CH],
                                           float y, int bxo, int byo,
                                           const unsigned (&colmask)[CH],
                                           const bool (&in_tile)[CH],
-                                          unsigned &rm) {
+                                          float &rmf) {
     using S = EtbrShape<D, CH, RW, NW>;
     const int lane = threadIdx.x & 31;
     const int band = (threadIdx.x >> 5) * RW;
@@ -487,10 +494,14 @@ __device__ __forceinline__ void etbr_band(float4 (&u)[RW][CH],
                 const bool tile_row = row >= D && row < D + S::TY;
                 if (in_tile[c] && tile_row && row_ok) {
                     const unsigned m = colmask[c];
-                    if (m & 1u) rm = max(rm, change_bits(nv.x, cur.x));
-                    if (m & 2u) rm = max(rm, change_bits(nv.y, cur.y));
-                    if (m & 4u) rm = max(rm, change_bits(nv.z, cur.z));
-                    if (m & 8u) rm = max(rm, change_bits(nv.w, cur.w));
+                    const float2 d01 = __fadd2_rn(make_float2(nv.x, nv.y),
+                                                  make_float2(-cur.x, -cur.y));
+                    const float2 d23 = __fadd2_rn(make_float2(nv.z, nv.w),
+                                                  make_float2(-cur.z, -cur.w));
+                    if (m & 1u) rmf = max_nan_abs(rmf, d01.x);
+                    if (m & 2u) rmf = max_nan_abs(rmf, d01.y);
+                    if (m & 4u) rmf = max_nan_abs(rmf, d23.x);
+                    if (m & 8u) rmf = max_nan_abs(rmf, d23.y);
                 }
             }
             if (EDGE) nv = hold4(nv, cur, row_ok, colmask[c]);
@@ -544,6 +555,7 @@ __device__ __forceinline__ void etbr_sweeps(float4 (&u)[RW][CH],
         colmask[c] = EDGE ? m : 0xfu;
         in_tile[c] = bx >= S::HX && bx < S::HX + S::TX;
     }
+    float rmf = __uint_as_float(rm);
     // This band's own slots (2*warp: top row, 2*warp + 1: bottom row) and
     // those of the rows next to it, at parity 0; parity 1 is XROWS rows on.
     float *own = xb + (2 * warp + 1) * S::BX + col;
@@ -574,20 +586,22 @@ __device__ __forceinline__ void etbr_sweeps(float4 (&u)[RW][CH],
 
     if (band + RW > 1 && band < S::BY - 1)
         etbr_band<D, CH, RW, NW, FAST, EDGE, FUSED, false>(
-            u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rm);
+            u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rmf);
     exchange(0);
 #pragma unroll 1
     for (int s = 1; s < D - 1; ++s) {
         if (band + RW > s + 1 && band < S::BY - 1 - s)
             etbr_band<D, CH, RW, NW, FAST, EDGE, false, false>(
                 u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile,
-                rm);
+                rmf);
         exchange(s);
     }
     if (band + RW > D && band < S::BY - D)
         etbr_band<D, CH, RW, NW, FAST, EDGE, false, true>(
-            u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rm);
+            u, b, hn, hs, out, n, ld, r, d, y, bxo, byo, colmask, in_tile, rmf);
+    rm = __float_as_uint(rmf);
 }
+
 
 // Persistent kernel with register-resident bands: block k handles tiles k,
 // k + gridDim.x, ... One staging set: the next tile's boxes are loaded as
