@@ -11,10 +11,11 @@ Default workload: N = 2048 (ring included), r = 10, Gaussian source
 σ = N/16, amplitude 100, 10 time steps, tol 1e-5, M = 8; strategies SYNC and
 EXACT_TEMPORAL_BLOCKED with D = 2, 4, 8; convergence loop on the device
 (--control host: one host round trip per check instead). `value` is the GLUP/s (interior
-points × sweeps ÷ time) of the fastest strategy; every strategy's figures
-are under "strategies". All strategies perform the same sweeps (exact
-temporal blocking is bit-identical to SYNC), so their GLUP/s compare
-time-to-solution directly.
+points × sweeps ÷ time) of the strategy with the shortest ten-step
+time-to-solution; every strategy's figures are under "strategies". SYNC and
+EXACT_TEMPORAL_BLOCKED perform the same sweeps (exact temporal blocking is
+bit-identical to SYNC), so their GLUP/s compare time-to-solution directly;
+BLOCK_ASYNC needs s times the sweeps and its GLUP/s counts them.
 
 Usage:
   python bench.py [--steps K] [--warmup W] [--workload NAME]
@@ -285,8 +286,9 @@ def run_ours(args):
         barrier()
         wall = time.perf_counter() - t_wall0
 
-    # headline: fastest strategy
-    best = max(results, key=lambda t: results[t]["glups"])
+    # headline: the shortest ten-step time-to-solution (block-async strategies
+    # sweep more often, so their GLUP/s is not a time-to-solution ranking)
+    best = min(results, key=lambda t: results[t]["ms_per_solve_median"])
     base = results.get("sync")
     for tok, res in results.items():
         if base:
@@ -388,6 +390,8 @@ def kernel_name(tok):
         name = ("k_etbr" if kw["depth"] in (4, 8, 16) and kw.get("tile", (0, 0)) == (0, 0)
                 else "k_etb")
         return f"{name} (D={kw['depth']})"
+    if kw.get("tile", (0, 0)) in ((0, 0), (32, 8)) and not kw.get("overlap"):
+        return f"k_bar (D={kw['depth']})"  # 32 x 8 tiles held in registers
     return f"k_ba / k_block_async (D={kw['depth']})"
 
 

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtbjacobi.so")
 SOURCES = ["kernels_sync.cu", "kernels_tiled.cu", "kernels_etb.cu",
-           "kernels_ba.cu", "fastdiv.cu", "jacobi_abi.cu", "residual_noalloc.cu",
+           "kernels_ba.cu", "kernels_bar.cu", "fastdiv.cu", "jacobi_abi.cu", "residual_noalloc.cu",
            "adapt.cu"]
 HEADERS = [os.path.join(CSRC, "jacobi_kernels.cuh"),
            os.path.join(ROOT, "include", "jacobi.h")]

@@ -247,8 +247,8 @@ cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
             return launch_sweep_etb(h->g, h->tc, map_src, &h->map_b, dst,
                                     h->dev_out, ctl, s);
         default:
-            return launch_sweep_ba(h->g, h->tc, map_src, &h->map_b, dst,
-                                   h->dev_out, ctl, s);
+            return launch_sweep_ba(h->g, h->tc, map_src, &h->map_b, src,
+                                   h->b, dst, h->dev_out, ctl, s);
     }
 }
 

@@ -68,6 +68,62 @@ __device__ __forceinline__ float jacobi_update(float uw, float ue, float un,
     return div_d<FAST>(num, d, y);
 }
 
+// ---------------------------------------------------------------------------
+// Row-chunk forms used by the tiled kernels: one lane holds a float4 chunk
+// of a row.
+// ---------------------------------------------------------------------------
+// J for the four cells of a float4 chunk: n4, c4, s4 the rows above, at and
+// below, w/e the cells west of .x and east of .w.
+template <bool FAST>
+__device__ __forceinline__ float4 update4_we(float4 n4, float4 c4, float4 s4,
+                                             float4 b4, float w, float e,
+                                             float r, float d, float y) {
+    if (FAST) {
+        // Same operations, same order, mostly two cells per instruction:
+        // ((W+E) + (N+S)) * r + b, then the fixed-divisor division. The
+        // product r * s is formed with scalar round-to-nearest multiplies:
+        // a packed multiply feeding a packed add can be fused into one
+        // multiply-add by the compiler, which would change the rounding.
+        const float2 d2 = make_float2(d, d), y2 = make_float2(y, y);
+        const float2 h01 = make_float2(__fadd_rn(w, c4.y), __fadd_rn(c4.x, c4.z));
+        const float2 h23 = make_float2(__fadd_rn(c4.y, c4.w), __fadd_rn(c4.z, e));
+        const float2 v01 = __fadd2_rn(make_float2(n4.x, n4.y), make_float2(s4.x, s4.y));
+        const float2 v23 = __fadd2_rn(make_float2(n4.z, n4.w), make_float2(s4.z, s4.w));
+        const float2 s01 = __fadd2_rn(h01, v01), s23 = __fadd2_rn(h23, v23);
+        const float2 rs01 = make_float2(__fmul_rn(r, s01.x), __fmul_rn(r, s01.y));
+        const float2 rs23 = make_float2(__fmul_rn(r, s23.x), __fmul_rn(r, s23.y));
+        const float2 num01 = __fadd2_rn(make_float2(b4.x, b4.y), rs01);
+        const float2 num23 = __fadd2_rn(make_float2(b4.z, b4.w), rs23);
+        const float2 q01 = div2_fixed(num01, d2, y2);
+        const float2 q23 = div2_fixed(num23, d2, y2);
+        return make_float4(q01.x, q01.y, q23.x, q23.y);
+    }
+    float4 o;
+    o.x = jacobi_update<false>(w, c4.y, n4.x, s4.x, b4.x, r, d, y);
+    o.y = jacobi_update<false>(c4.x, c4.z, n4.y, s4.y, b4.y, r, d, y);
+    o.z = jacobi_update<false>(c4.y, c4.w, n4.z, s4.z, b4.z, r, d, y);
+    o.w = jacobi_update<false>(c4.z, e, n4.w, s4.w, b4.w, r, d, y);
+    return o;
+}
+
+// Keep the old value where the cell is not an interior grid cell.
+__device__ __forceinline__ float4 hold4(float4 nv, float4 old, bool row_ok,
+                                        unsigned colmask) {
+    float4 o;
+    o.x = (row_ok && (colmask & 1u)) ? nv.x : old.x;
+    o.y = (row_ok && (colmask & 2u)) ? nv.y : old.y;
+    o.z = (row_ok && (colmask & 4u)) ? nv.z : old.z;
+    o.w = (row_ok && (colmask & 8u)) ? nv.w : old.w;
+    return o;
+}
+
+// max(a, |x|) that returns NaN when either is NaN.
+__device__ __forceinline__ float max_nan_abs(float a, float x) {
+    float o;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(o) : "f"(a), "f"(fabsf(x)));
+    return o;
+}
+
 // Exhaustive check of div_fixed against __fdiv_rn for one d: counts the
 // finite float32 numerators whose quotients differ in any bit. `count` is a
 // device word (set to 0 by the caller). Launch fastdiv_verify_launch.
@@ -343,13 +399,22 @@ cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
 int ba_configure(int n, int depth, int tile_x, int tile_y, int overlap_x,
                  int overlap_y, TileConf *tc);
 cudaError_t prepare_sweep_ba(const TileConf &tc);
+// src / b: the launch's input iterate and the right-hand side (raw
+// pointers, for the register-resident kernel; the others use the maps).
 cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const CUtensorMap *map_src,
-                            const CUtensorMap *map_b, float *out,
-                            ResidualOut *status, const LaunchCtl &ctl,
-                            cudaStream_t stream);
+                            const CUtensorMap *map_b, const float *src,
+                            const float *b, float *out, ResidualOut *status,
+                            const LaunchCtl &ctl, cudaStream_t stream);
 // Blocks of one launch of a tiled strategy (size of the fused partials).
 int tiled_blocks(const GridDesc &g, const TileConf &tc);
+// Register-resident block-asynchronous kernel for 32 x 8 tiles
+// (kernels_bar.cu): tc.stream = 2, one warp per strip of four tiles.
+bool ba_reg_configure(int n, TileConf *tc);
+cudaError_t prepare_sweep_ba_reg();
+cudaError_t launch_sweep_ba_reg(const GridDesc &g, const TileConf &tc,
+                                const float *src, const float *b, float *out,
+                                const LaunchCtl &ctl, cudaStream_t stream);
 // Streaming block-asynchronous kernel (kernels_ba.cu).
 bool ba_stream_configure(int n, TileConf *tc);
 cudaError_t prepare_sweep_ba_stream(const TileConf &tc);

@@ -111,16 +111,6 @@ __device__ __forceinline__ float4 update4(float4 n4, float4 c4, float4 s4,
     return o;
 }
 
-__device__ __forceinline__ float4 hold4(float4 nv, float4 old, bool row_ok,
-                                        unsigned colmask) {
-    float4 o;
-    o.x = (row_ok && (colmask & 1u)) ? nv.x : old.x;
-    o.y = (row_ok && (colmask & 2u)) ? nv.y : old.y;
-    o.z = (row_ok && (colmask & 4u)) ? nv.z : old.z;
-    o.w = (row_ok && (colmask & 8u)) ? nv.w : old.w;
-    return o;
-}
-
 template <int CH, int RW, int NW, bool FAST, bool EDGE, bool FUSED>
 __device__ __forceinline__ void ba_sweeps(const float *sA, float *sB, float *sC,
                                           const float4 (&breg)[RW][CH],

@@ -117,51 +117,6 @@ __device__ __forceinline__ void sts4(float *p, float4 v) {
     *reinterpret_cast<float4 *>(p) = v;
 }
 
-// J for the four cells of a float4 chunk: n4, c4, s4 the rows above, at and
-// below, w/e the cells west of .x and east of .w.
-template <bool FAST>
-__device__ __forceinline__ float4 update4(float4 n4, float4 c4, float4 s4,
-                                          float4 b4, float w, float e, float r,
-                                          float d, float y) {
-    if (FAST) {
-        // Same operations, same order, mostly two cells per instruction:
-        // ((W+E) + (N+S)) * r + b, then the fixed-divisor division. The
-        // product r * s is formed with scalar round-to-nearest multiplies:
-        // a packed multiply feeding a packed add can be fused into one
-        // multiply-add by the compiler, which would change the rounding.
-        const float2 d2 = make_float2(d, d), y2 = make_float2(y, y);
-        const float2 h01 = make_float2(__fadd_rn(w, c4.y), __fadd_rn(c4.x, c4.z));
-        const float2 h23 = make_float2(__fadd_rn(c4.y, c4.w), __fadd_rn(c4.z, e));
-        const float2 v01 = __fadd2_rn(make_float2(n4.x, n4.y), make_float2(s4.x, s4.y));
-        const float2 v23 = __fadd2_rn(make_float2(n4.z, n4.w), make_float2(s4.z, s4.w));
-        const float2 s01 = __fadd2_rn(h01, v01), s23 = __fadd2_rn(h23, v23);
-        const float2 rs01 = make_float2(__fmul_rn(r, s01.x), __fmul_rn(r, s01.y));
-        const float2 rs23 = make_float2(__fmul_rn(r, s23.x), __fmul_rn(r, s23.y));
-        const float2 num01 = __fadd2_rn(make_float2(b4.x, b4.y), rs01);
-        const float2 num23 = __fadd2_rn(make_float2(b4.z, b4.w), rs23);
-        const float2 q01 = div2_fixed(num01, d2, y2);
-        const float2 q23 = div2_fixed(num23, d2, y2);
-        return make_float4(q01.x, q01.y, q23.x, q23.y);
-    }
-    float4 o;
-    o.x = jacobi_update<false>(w, c4.y, n4.x, s4.x, b4.x, r, d, y);
-    o.y = jacobi_update<false>(c4.x, c4.z, n4.y, s4.y, b4.y, r, d, y);
-    o.z = jacobi_update<false>(c4.y, c4.w, n4.z, s4.z, b4.z, r, d, y);
-    o.w = jacobi_update<false>(c4.z, e, n4.w, s4.w, b4.w, r, d, y);
-    return o;
-}
-
-// Keep the old value where the cell is not an interior grid cell.
-__device__ __forceinline__ float4 hold4(float4 nv, float4 old, bool row_ok,
-                                        unsigned colmask) {
-    float4 o;
-    o.x = (row_ok && (colmask & 1u)) ? nv.x : old.x;
-    o.y = (row_ok && (colmask & 2u)) ? nv.y : old.y;
-    o.z = (row_ok && (colmask & 4u)) ? nv.z : old.z;
-    o.w = (row_ok && (colmask & 8u)) ? nv.w : old.w;
-    return o;
-}
-
 // One sweep of one tile. RESID: also reduce |J(u) - u| (first sweep of a
 // fused launch); LAST: write the tile to global memory instead of to dst.
 template <int D, int CH, int RW, int NW, bool FAST, bool EDGE, bool RESID,
@@ -207,7 +162,7 @@ __device__ __forceinline__ void etb_sweep(const float *src, float *dst, int s,
         for (int c = 0; c < CH; ++c) {
             const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
             const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
-            float4 nv = update4<FAST>(nr[c], cr[c], sr[c], breg[j][c], w, e, r,
+            float4 nv = update4_we<FAST>(nr[c], cr[c], sr[c], breg[j][c], w, e, r,
                                       d, y);
             if (RESID) {
                 const bool tile_row = row >= D && row < D + S::TY;
@@ -427,13 +382,6 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
 // the last) stay zero; the cells that read them lie outside the region that
 // is still exact.
 // ---------------------------------------------------------------------------
-// max(a, |x|) that returns NaN when either is NaN.
-__device__ __forceinline__ float max_nan_abs(float a, float x) {
-    float o;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(o) : "f"(a), "f"(fabsf(x)));
-    return o;
-}
-
 template <int D, int CH, int RW, int NW>
 struct EtbrShape {
     static constexpr int BX = 128 * CH;
@@ -489,7 +437,7 @@ __device__ __forceinline__ void etbr_band(float4 (&u)[RW][CH],
             const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
             const float4 cur = u[j][c];
             const float4 nxt = (j + 1 < RW) ? u[j + 1 < RW ? j + 1 : j][c] : hs[c];
-            float4 nv = update4<FAST>(prev[c], cur, nxt, b[j][c], w, e, r, d, y);
+            float4 nv = update4_we<FAST>(prev[c], cur, nxt, b[j][c], w, e, r, d, y);
             if (RESID) {
                 const bool tile_row = row >= D && row < D + S::TY;
                 if (in_tile[c] && tile_row && row_ok) {

@@ -317,23 +317,28 @@ int ba_configure(int n, int depth, int tile_x, int tile_y, int overlap_x,
     tc->stream = tc->ch = tc->sx = tc->sy = 0;
     tc->grid_x = subdomain_count(n - 2, tile_x, overlap_x);
     tc->grid_y = subdomain_count(n - 2, tile_y, overlap_y);
-    // The streaming kernel takes every non-overlapping shape it can fit; the
-    // generic one-tile-per-block kernel below is kept for the rest.
+    // Non-overlapping 32 x 8 tiles (the default) are held in registers; the
+    // streaming kernel takes every other non-overlapping shape it can fit;
+    // the generic one-tile-per-block kernel below is kept for the rest.
+    if (overlap_x == 0 && overlap_y == 0 && ba_reg_configure(n, tc)) return 0;
     if (overlap_x == 0 && overlap_y == 0 && ba_stream_configure(n, tc)) return 0;
     return finish_conf(tc);
 }
 
 cudaError_t prepare_sweep_ba(const TileConf &tc) {
+    if (tc.stream == 2) return prepare_sweep_ba_reg();
     if (tc.stream) return prepare_sweep_ba_stream(tc);
     return prepare_tiled(tc);
 }
 
 cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const CUtensorMap *map_src,
-                            const CUtensorMap *map_b, float *out,
-                            ResidualOut *status, const LaunchCtl &ctl,
-                            cudaStream_t stream) {
+                            const CUtensorMap *map_b, const float *src,
+                            const float *b, float *out, ResidualOut *status,
+                            const LaunchCtl &ctl, cudaStream_t stream) {
     unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
+    if (tc.stream == 2)
+        return launch_sweep_ba_reg(g, tc, src, b, out, ctl, stream);
     if (tc.stream)
         return launch_sweep_ba_stream(g, tc, map_src, map_b, out, err, ctl,
                                       stream);
