@@ -3,7 +3,8 @@
 Meant for profilers (a few launches, bounded memory):
   python -m temporal_blocked_jacobi_gb300.profile_case --n 8192 --r 100 \
       --source gauss --strategy etb8 --launches 4 --residuals 1
-Strategy tokens: sync | etbD | baD | baD@TXxTY. Prints the mean launch time
+Strategy tokens: sync | syncu (unfused right-hand side) | etbD | baD |
+baDoO (overlap O) | any of them with @TXxTY. Prints the mean launch time
 measured with CUDA events on the solver's stream.
 """
 from __future__ import annotations
@@ -33,8 +34,13 @@ def main(argv=None):
         tile = tuple(int(v) for v in t.lower().split("x"))
     if tok == "sync":
         kw = dict(strategy="sync", depth=1)
+    elif tok == "syncu":  # unfused right-hand side
+        kw = dict(strategy="sync", depth=1, rhs="unfused")
     elif tok.startswith("etb"):
         kw = dict(strategy="etb", depth=int(tok[3:]))
+    elif tok.startswith("ba") and "o" in tok:  # baDoO: overlap O both ways
+        depth, ov = tok[2:].split("o")
+        kw = dict(strategy="ba", depth=int(depth), overlap=(int(ov), int(ov)))
     elif tok.startswith("ba"):
         kw = dict(strategy="ba", depth=int(tok[2:]))
     else:
