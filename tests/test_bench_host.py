@@ -70,3 +70,23 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["unit"] == "GLUP/s"
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_headline_is_shortest_time_to_solution():
+    """Block-async needs more sweeps, so its GLUP/s can exceed that of a
+    strategy that reaches the solution sooner; the headline follows time."""
+    results = {
+        "sync": {"ms_per_solve_median": 160.0, "glups": 430.0},
+        "etb8": {"ms_per_solve_median": 44.5, "glups": 1550.0},
+        "ba16": {"ms_per_solve_median": 79.6, "glups": 2311.0},
+    }
+    assert bench.headline(results) == "etb8"
+
+
+def test_kernel_names_follow_default_shapes():
+    assert bench.kernel_name("etb4").startswith("k_etbr")
+    assert bench.kernel_name("etb2").startswith("k_etb ")
+    assert bench.kernel_name("etb8@112x48").startswith("k_etb ")
+    assert bench.kernel_name("ba8").startswith("k_bar")
+    assert bench.kernel_name("ba8@32x16").startswith("k_ba ")
+    assert bench.kernel_name("ba8o4").startswith("k_ba ")
