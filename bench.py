@@ -62,8 +62,10 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
 def parse_strategy(tok: str):
-    """'sync' | 'syncu' | 'etbD' | 'baD' | 'baDoO' | 'gascD' | 'gdescD' |
-    'gfbD', each optionally '@TXxTY' -> kwargs for jacobi.Solver. 'syncu':
+    """'sync' | 'syncu' | 'etbD' | 'etbDp' | 'baD' | 'baDoO' | 'gascD' |
+    'gdescD' | 'gfbD', each optionally '@TXxTY' -> kwargs for jacobi.Solver.
+    'etbDp': EXACT_TEMPORAL_BLOCKED under persistent control (one cooperative
+    launch per time step); 'syncu':
     SYNC with the unfused right-hand side; 'baDoO': BLOCK_ASYNC on subdomains
     overlapping by O cells in both directions; 'gasc', 'gdesc', 'gfb':
     BLOCK_ASYNC with that depth controller and D up to the given depth (host
@@ -86,6 +88,9 @@ def parse_strategy(tok: str):
         depth, ov = tok[2:].split("o")
         return dict(strategy="ba", depth=int(depth), tile=tile,
                     overlap=(int(ov), int(ov)))
+    if tok.startswith("etb") and tok.endswith("p"):  # 'etbDp': persistent control
+        return dict(strategy="etb", depth=int(tok[3:-1]), tile=tile,
+                    control="persistent")
     for prefix, name in (("etb", "etb"), ("ba", "ba")):
         if tok.startswith(prefix):
             return dict(strategy=name, depth=int(tok[len(prefix):]), tile=tile)
@@ -394,6 +399,8 @@ def kernel_name(tok):
         # shared memory for D = 2
         name = ("k_etbr" if kw["depth"] in (4, 8, 16) and kw.get("tile", (0, 0)) == (0, 0)
                 else "k_etb")
+        if kw.get("control") == "persistent":
+            name = "k_etbp"  # the whole step in one cooperative launch
         return f"{name} (D={kw['depth']})"
     if kw.get("tile", (0, 0)) in ((0, 0), (32, 8)) and not kw.get("overlap"):
         return f"k_bar (D={kw['depth']})"  # 32 x 8 tiles held in registers

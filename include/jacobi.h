@@ -69,7 +69,18 @@ typedef enum {
      * anyway) and its last block applies the stopping rule and sets the loop
      * condition; launches queued after the stop return at once. Same
      * iterates, same sweep counts, same statuses as JACOBI_CONTROL_HOST. */
-    JACOBI_CONTROL_DEVICE = 1
+    JACOBI_CONTROL_DEVICE = 1,
+    /* EXACT_TEMPORAL_BLOCKED only, with a register-resident tile shape (the
+     * default tiles of D = 4, 8 and 16; other shapes return
+     * JACOBI_ERR_UNSUPPORTED): a whole time step is one cooperative kernel
+     * launch. Its blocks sweep the tiles D sweeps at a time and meet at a
+     * grid-wide barrier between those rounds instead of at a kernel
+     * boundary; the first round of each check interval reduces the residual
+     * of its input and the last block to reach the following barrier applies
+     * the stopping rule. Every barrier wait gives up after about a second
+     * and the step then returns JACOBI_ERR_CUDA. Same iterates, sweep counts
+     * and statuses as the other controls. */
+    JACOBI_CONTROL_PERSISTENT = 2
 } jacobi_control_t;
 
 /* How the kernels divide by d = 1 + 4r. Both give the correctly rounded

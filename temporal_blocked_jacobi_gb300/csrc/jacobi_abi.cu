@@ -174,8 +174,14 @@ int check_config(jacobi_handle_t *h, const jacobi_config_t &c) {
         return fail(h, JACOBI_ERR_INVALID_ARG, "tol must be finite and >= 0");
     if (c.max_sweeps < 1)
         return fail(h, JACOBI_ERR_INVALID_ARG, "max_sweeps must be >= 1");
-    if (c.control != JACOBI_CONTROL_HOST && c.control != JACOBI_CONTROL_DEVICE)
+    if (c.control != JACOBI_CONTROL_HOST && c.control != JACOBI_CONTROL_DEVICE &&
+        c.control != JACOBI_CONTROL_PERSISTENT)
         return fail(h, JACOBI_ERR_INVALID_ARG, "unknown control %d", c.control);
+    if (c.control == JACOBI_CONTROL_PERSISTENT &&
+        c.strategy != JACOBI_EXACT_TEMPORAL_BLOCKED)
+        return fail(h, JACOBI_ERR_UNSUPPORTED,
+                    "JACOBI_CONTROL_PERSISTENT is provided for "
+                    "EXACT_TEMPORAL_BLOCKED only");
     switch (c.strategy) {
         case JACOBI_SYNC:
             if (c.depth != 1)
@@ -340,12 +346,51 @@ cudaError_t capture_body(jacobi_handle_t *h, LoopState *st,
     return e;
 }
 
+// Persistent control: the one cooperative launch that runs the step whose
+// state is `st`, from u (its answer lands in u or u_alt, LoopState::where).
+cudaError_t enqueue_persistent(jacobi_handle_t *h, LoopState *st,
+                               cudaStream_t s) {
+    const LaunchCtl c = loop_ctl(h, st, true, 0, cudaGraphConditionalHandle{});
+    return launch_etb_persistent(h->g, h->tc, &h->map_u, &h->map_alt, &h->map_b,
+                                 h->u, h->u_alt, c.lp, h->launches_per_check, s);
+}
+
+// Persistent control: record the graph of one time step,
+//   reset(LoopState) -> bmax of b -> persistent step -> copy LoopState to
+//   the host.
+int record_step_persistent(jacobi_handle_t *h) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(h->capture, cudaStreamCaptureModeThreadLocal);
+    auto check = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+        return e == cudaSuccess;
+    };
+    if (e == cudaSuccess) {
+        check(launch_loop_reset(h->loop, nullptr, h->capture));
+        check(launch_bnorm(h->g, h->u, h->b, h->loop, h->capture));
+        check(enqueue_persistent(h, h->loop, h->capture));
+        check(cudaMemcpyAsync(h->loop_host, h->loop, sizeof(LoopState),
+                              cudaMemcpyDeviceToHost, h->capture));
+        cudaError_t e2 = cudaStreamEndCapture(h->capture, &graph);
+        check(e2);
+    }
+    if (e == cudaSuccess) check(cudaGraphInstantiate(&h->step, graph, 0));
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, JACOBI_ERR_CUDA, "recording the persistent step graph: %s",
+                    cudaGetErrorString(e));
+    }
+    return JACOBI_OK;
+}
+
 // Device control: record the graph of one time step,
 //   reset(LoopState) -> bmax of b -> WHILE(cond) { body } -> copy LoopState
 //   to the host,
 // where the body is intervals_per_iteration() check intervals starting from u,
 // each with a fused first launch and the rest honouring the stop flag.
 int record_step(jacobi_handle_t *h) {
+    if (h->cfg.control == JACOBI_CONTROL_PERSISTENT) return record_step_persistent(h);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaGraphCreate(&graph, 0);
     cudaGraphConditionalHandle cond{};
@@ -416,7 +461,61 @@ int record_step(jacobi_handle_t *h) {
 //   [-> settle: answer back into u, when intervals have an odd launch count]
 // and a single copy of all steps' states to pinned memory ends the graph.
 // A step whose predecessor did not converge is skipped on the device.
+// Persistent control, whole run: per step the right-hand side, the reset of
+// that step's state (skipped after a failed step), bmax, the persistent
+// step and the settle kernel (the answer may sit in u_alt), then one copy of
+// all step states to pinned memory.
+int record_run_persistent(jacobi_handle_t *h, const float *g, int steps) {
+    if (h->run) cudaGraphExecDestroy(h->run);
+    h->run = nullptr;
+    h->run_g = nullptr;
+    h->run_steps = 0;
+    if (steps > h->run_cap) {
+        if (h->run_states) cudaFree(h->run_states);
+        if (h->run_states_host) cudaFreeHost(h->run_states_host);
+        h->run_states = nullptr;
+        h->run_states_host = nullptr;
+        h->run_cap = 0;
+        TBJ_CUDA(h, cudaMalloc(&h->run_states, sizeof(LoopState) * steps));
+        TBJ_CUDA(h, cudaMallocHost(&h->run_states_host, sizeof(LoopState) * steps));
+        h->run_cap = steps;
+    }
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(h->capture, cudaStreamCaptureModeThreadLocal);
+    auto check = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+        return e == cudaSuccess;
+    };
+    if (e == cudaSuccess) {
+        for (int s = 0; s < steps && e == cudaSuccess; ++s) {
+            LoopState *st = h->run_states + s;
+            check(launch_rhs(h->g, h->u, g, h->b, h->capture));
+            check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture));
+            check(launch_bnorm(h->g, h->u, h->b, st, h->capture));
+            check(enqueue_persistent(h, st, h->capture));
+            check(launch_settle(h->g, st, h->u_alt, h->u, h->capture));
+        }
+        check(cudaMemcpyAsync(h->run_states_host, h->run_states,
+                              sizeof(LoopState) * steps, cudaMemcpyDeviceToHost,
+                              h->capture));
+        cudaError_t e2 = cudaStreamEndCapture(h->capture, &graph);
+        check(e2);
+    }
+    if (e == cudaSuccess) check(cudaGraphInstantiate(&h->run, graph, 0));
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, JACOBI_ERR_CUDA, "recording the persistent run graph: %s",
+                    cudaGetErrorString(e));
+    }
+    h->run_g = g;
+    h->run_steps = steps;
+    return JACOBI_OK;
+}
+
 int record_run(jacobi_handle_t *h, const float *g, int steps) {
+    if (h->cfg.control == JACOBI_CONTROL_PERSISTENT)
+        return record_run_persistent(h, g, steps);
     if (h->run) cudaGraphExecDestroy(h->run);
     h->run = nullptr;
     h->run_g = nullptr;
@@ -610,11 +709,18 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
                         ? prepare_sweep_etb(h->tc, h->g.n)
                         : prepare_sweep_ba(h->tc));
     }
+    if (c.control == JACOBI_CONTROL_PERSISTENT) {
+        if (!etb_persistent_ok(h->tc))
+            return fail(h, JACOBI_ERR_UNSUPPORTED,
+                        "JACOBI_CONTROL_PERSISTENT needs a tile shape held in "
+                        "registers (the default tile of D = 4, 8 or 16)");
+        TBJ_CUDA(h, prepare_etb_persistent(h->tc, h->g.n));
+    }
     h->per_launch = c.strategy == JACOBI_SYNC ? 1 : c.depth;
     h->interval = (long long)c.check_every /
                   gcd_ll(c.check_every, h->per_launch) * h->per_launch;
     h->launches_per_check = h->interval / h->per_launch;
-    if (c.control == JACOBI_CONTROL_DEVICE) return record_step(h);
+    if (c.control != JACOBI_CONTROL_HOST) return record_step(h);
     if ((rc = record_batch(h, 0, &h->batch[0]))) return rc;
     if (h->launches_per_check % 2 == 1)
         if ((rc = record_batch(h, 1, &h->batch[1]))) return rc;
@@ -800,6 +906,8 @@ static int check_b_mode(jacobi_handle_t *h) {
 // kernel. A skipped step runs one iteration of no-ops.
 static long long device_step_launches(const jacobi_handle_t *h,
                                       const LoopState &st) {
+    // persistent: reset, bmax and the one cooperative launch
+    if (h->cfg.control == JACOBI_CONTROL_PERSISTENT) return 3;
     const long long per_body = intervals_per_iteration(h->launches_per_check, h->g.n);
     const long long checks =
         st.status == kStepSkipped ? 1 : st.result_k / h->interval + 1;
@@ -814,6 +922,10 @@ static long long device_step_outcome(jacobi_handle_t *h, const LoopState &st) {
     if (st.err & ERR_TMA_TIMEOUT)
         return fail(h, JACOBI_ERR_CUDA,
                     "a TMA load did not complete within its wait limit");
+    if (st.err & ERR_SYNC_TIMEOUT)
+        return fail(h, JACOBI_ERR_CUDA,
+                    "a grid barrier of the persistent step did not complete "
+                    "within its wait limit");
     switch (st.status) {
         case 0:
             return st.result_k;
@@ -855,7 +967,8 @@ static long long run_device(jacobi_handle_t *h, const float *g, int steps,
     TBJ_CUDA(h, cudaGraphLaunch(h->run, h->stream));
     TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
     h->b_mode = h->cfg.rhs;
-    const bool settle_needed = h->launches_per_check % 2 == 1;
+    const bool settle_needed = h->launches_per_check % 2 == 1 ||
+                               h->cfg.control == JACOBI_CONTROL_PERSISTENT;
     long long total = 0;
     for (int s = 0; s < steps; ++s) {
         const LoopState st = h->run_states_host[s];
@@ -963,7 +1076,7 @@ long long jacobi_solve_step(jacobi_handle_t *h) {
         if (rc) return rc;
         return solve_step_adaptive(h);
     }
-    if (h->cfg.control == JACOBI_CONTROL_DEVICE) {
+    if (h->cfg.control != JACOBI_CONTROL_HOST) {
         int rc = settle(h);
         if (rc) return rc;
         return solve_step_device(h);
@@ -1039,7 +1152,7 @@ long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
                      long long *sweeps_per_step) {
     if (!h) return JACOBI_ERR_INVALID_ARG;
     if (steps < 0) return fail(h, JACOBI_ERR_INVALID_ARG, "steps must be >= 0");
-    if (steps > 0 && h->cfg.control == JACOBI_CONTROL_DEVICE && h->nlevels == 0) {
+    if (steps > 0 && h->cfg.control != JACOBI_CONTROL_HOST && h->nlevels == 0) {
         if (!g || !aligned16(g))
             return fail(h, JACOBI_ERR_INVALID_ARG,
                         "g must be a 16-byte aligned buffer");

@@ -134,7 +134,8 @@ float reciprocal_rn(float d);
 
 // Error bits written by kernels into the handle's status word.
 enum : unsigned {
-    ERR_TMA_TIMEOUT = 1u,  // an mbarrier wait for a TMA load gave up
+    ERR_TMA_TIMEOUT = 1u,   // an mbarrier wait for a TMA load gave up
+    ERR_SYNC_TIMEOUT = 2u,  // a grid-wide barrier wait gave up
 };
 
 // Parameters common to all sweep kernels.
@@ -189,6 +190,9 @@ struct LoopState {
     int where;            // buffer holding the answer: 0 u, 1 u_alt
     unsigned rbits;       // running max of |J(u) - u| (bit pattern) of the
                           // current check; 0 between checks
+    unsigned bar_arrive;  // persistent kernel: blocks arrived at its grid
+                          // barriers so far (all rounds)
+    unsigned bar_epoch;   // persistent kernel: barriers completed
 };
 
 struct LoopParams {
@@ -390,6 +394,20 @@ cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              const CUtensorMap *map_b, float *out,
                              ResidualOut *status, const LaunchCtl &ctl,
                              cudaStream_t stream);
+
+// Persistent exact temporal blocking (JACOBI_CONTROL_PERSISTENT): one
+// cooperative launch runs a whole time step. `tc` must be a register-resident
+// shape (etb_persistent_ok). prepare_etb_persistent raises the shared-memory
+// limit and sizes the grid to the blocks that fit on the GPU at once.
+bool etb_persistent_ok(const TileConf &tc);
+cudaError_t prepare_etb_persistent(TileConf &tc, int n);
+cudaError_t launch_etb_persistent(const GridDesc &g, const TileConf &tc,
+                                  const CUtensorMap *map_u,
+                                  const CUtensorMap *map_alt,
+                                  const CUtensorMap *map_b, float *u,
+                                  float *u_alt, const LoopParams &lp,
+                                  long long rounds_per_check,
+                                  cudaStream_t stream);
 
 // Block-asynchronous sweep (section 02 "Block-asynchronous"): one-cell
 // halo frozen at launch, all tile cells updated D times.

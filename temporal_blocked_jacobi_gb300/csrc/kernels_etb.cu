@@ -645,6 +645,204 @@ k_etbr(const __grid_constant__ CUtensorMap map_src,
     if (FUSED) fused_block_finish(rm, lp, fin_scratch);
 }
 
+// ---------------------------------------------------------------------------
+// Persistent exact temporal blocking (JACOBI_CONTROL_PERSISTENT). One
+// cooperative launch runs a whole time step: rounds of D sweeps over all
+// tiles, as k_etbr launches would, separated by a grid-wide barrier instead
+// of a kernel boundary. Round q reads u (q even) or u_alt (q odd) and writes
+// the other. The first round of every check interval also reduces
+// max |J(u) - u| of its input; at the barrier after it, the last block to
+// arrive applies the stopping rule (loop_decide, the same as the device
+// loop's fused launch), and every block reads the outcome once released.
+// The answer is then the input of that round, as with the device loop.
+//
+// The barrier counts arrivals in LoopState::bar_arrive (all rounds) and
+// releases by advancing LoopState::bar_epoch; every wait gives up after
+// ~1 s and sets ERR_SYNC_TIMEOUT, so a block that cannot be scheduled ends
+// the step with an error instead of a hang. The launch is cooperative, so
+// all blocks are resident together or the launch fails.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid barrier number `round` (0, 1, ...). The last block to arrive runs
+// `last` before releasing the others. Returns the step's stop flag as seen
+// after the barrier (1 as well when the wait gave up).
+template <class F>
+__device__ __forceinline__ bool etbp_barrier(LoopState *st, unsigned round,
+                                             unsigned *s_flag, F last) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        bool ok = true;
+        __threadfence();
+        const unsigned target = (round + 1u) * gridDim.x;
+        if (atomicAdd(&st->bar_arrive, 1u) + 1u == target) {
+            __threadfence();  // every block's atomics and stores are visible
+            last();
+            __threadfence();
+            st_release_gpu(&st->bar_epoch, round + 1u);
+        } else {
+            unsigned spins = 0;
+            uint64_t t0 = 0;
+            while (ld_acquire_gpu(&st->bar_epoch) < round + 1u) {
+                if ((++spins & 255u) == 0u) {
+                    const uint64_t t = global_ns();
+                    if (t0 == 0) {
+                        t0 = t;
+                    } else if (t - t0 > 1000000000ull) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (!ok) atomicOr(&st->err, (unsigned)ERR_SYNC_TIMEOUT);
+        }
+        *s_flag = ok ? (unsigned)ld_acquire_gpu(reinterpret_cast<const unsigned *>(&st->stop))
+                     : 1u;
+        // The next round's TMA loads (async proxy) read what other blocks
+        // stored with ordinary stores before the barrier.
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncthreads();
+    return *s_flag != 0u;
+}
+
+template <int D, int CH, int RW, int NW, int MINB, bool FAST>
+__global__ void __launch_bounds__(32 * NW, MINB)
+k_etbp(const __grid_constant__ CUtensorMap map_u,
+       const __grid_constant__ CUtensorMap map_alt,
+       const __grid_constant__ CUtensorMap map_b, float *__restrict__ u,
+       float *__restrict__ u_alt, int n, long long ld, float r, float d,
+       float y, LoopParams lp, int rounds_per_check, int tiles_x, int tiles) {
+    using S = EtbrShape<D, CH, RW, NW>;
+    using L = EtbShape<D, CH, RW, NW, 1>;
+    __shared__ unsigned red[33];
+    __shared__ unsigned s_flag;
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + pad);
+    float *su = reinterpret_cast<float *>(smem_raw + pad + 128);
+    float *sb = su + S::BX * S::BY;
+    float *xb = sb + S::BX * S::BY;
+
+    const int tid = threadIdx.x;
+    LoopState *st = lp.state;
+    for (int k = tid; k < S::BX; k += 32 * NW)
+        for (int q = 0; q < 2; ++q) {
+            xb[q * S::XROWS * S::BX + k] = 0.f;
+            xb[(q * S::XROWS + S::XROWS - 1) * S::BX + k] = 0.f;
+        }
+    if (tid == 0) {
+        mbar_init(bar);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // A step whose predecessor failed is marked stopped before it starts.
+    if (*reinterpret_cast<volatile const int *>(&st->stop)) return;
+
+    const int lane = tid & 31, warp = tid >> 5;
+    const int band = warp * RW;
+    int i = 0;  // loads so far: load i completes mbarrier phase i
+    for (unsigned round = 0;; ++round) {
+        const bool from_alt = (round & 1u) != 0u;
+        const CUtensorMap *msrc = from_alt ? &map_alt : &map_u;
+        float *out = from_alt ? u : u_alt;
+        const bool fused = round % (unsigned)rounds_per_check == 0u;
+        unsigned rm = 0u;
+        bool failed = false;
+        if (tid == 0 && (int)blockIdx.x < tiles)
+            load_tile<L>(msrc, &map_b, bar, su, sb, blockIdx.x, tiles_x, D);
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const unsigned parity = (unsigned)i & 1u;
+            const bool ok = mbar_wait_parity(bar, parity);
+            if (__syncthreads_or(!ok)) {
+                // Let the load land (bounded) before the buffers are reused,
+                // report, and skip the rest of the round; the barrier below
+                // still sees this block, and the decision stops the step.
+                mbar_wait_parity(bar, parity);
+                if (tid == 0) atomicOr(&st->err, (unsigned)ERR_TMA_TIMEOUT);
+                failed = true;
+                ++i;
+                break;
+            }
+            float4 uu[RW][CH], bb[RW][CH], hn[CH], hs[CH];
+#pragma unroll
+            for (int j = 0; j < RW; ++j)
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    uu[j][c] = lds4(su + (band + j) * S::BX + 128 * c + 4 * lane);
+                    bb[j][c] = lds4(sb + (band + j) * S::BX + 128 * c + 4 * lane);
+                }
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                hn[c] = band > 0 ? lds4(su + (band - 1) * S::BX + 128 * c + 4 * lane)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                hs[c] = band + RW < S::BY
+                            ? lds4(su + (band + RW) * S::BX + 128 * c + 4 * lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            __syncthreads();  // staging consumed
+            if (tid == 0 && t + (int)gridDim.x < tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                load_tile<L>(msrc, &map_b, bar, su, sb, t + gridDim.x, tiles_x, D);
+            }
+            const int gx0 = (t % tiles_x) * S::TX, gy0 = (t / tiles_x) * S::TY;
+            const int bxo = gx0 - S::HX, byo = gy0 - D;
+            const bool edge = bxo < 1 || byo < 1 || bxo + S::BX > n - 1 ||
+                              byo + S::BY > n - 1;
+            if (fused) {
+                if (edge)
+                    etbr_sweeps<D, CH, RW, NW, FAST, true, true>(
+                        uu, bb, hn, hs, xb, out, n, ld, r, d, y, bxo, byo, rm);
+                else
+                    etbr_sweeps<D, CH, RW, NW, FAST, false, true>(
+                        uu, bb, hn, hs, xb, out, n, ld, r, d, y, bxo, byo, rm);
+            } else {
+                if (edge)
+                    etbr_sweeps<D, CH, RW, NW, FAST, true, false>(
+                        uu, bb, hn, hs, xb, out, n, ld, r, d, y, bxo, byo, rm);
+                else
+                    etbr_sweeps<D, CH, RW, NW, FAST, false, false>(
+                        uu, bb, hn, hs, xb, out, n, ld, r, d, y, bxo, byo, rm);
+            }
+        }
+        (void)failed;
+        if (fused) {
+            // This block's share of max |J(u) - u| of the round's input.
+            rm = warp_max_u(rm);
+            __syncthreads();
+            if (lane == 0) red[warp] = rm;
+            __syncthreads();
+            if (tid == 0) {
+                unsigned br = 0u;
+                for (int w = 0; w < NW; ++w) br = max(br, red[w]);
+                if (br) atomicMax(&st->rbits, br);
+            }
+        }
+        const bool stop = etbp_barrier(st, round, &s_flag, [&]() {
+            if (fused) {
+                LoopParams lq = lp;
+                lq.src_is_alt = from_alt ? 1 : 0;
+                const unsigned bits = atomicExch(&st->rbits, 0u);
+                loop_decide(lq, __fmul_rn(lp.d, __uint_as_float(bits)), st->bmax);
+            } else if (st->err) {
+                st->status = -2;  // JACOBI_ERR_CUDA
+                st->where = from_alt ? 0 : 1;
+                st->result_k = st->k;
+                st->stop = 1;
+            }
+        });
+        if (stop) break;
+    }
+}
+
 // Shapes per depth: {KIND, CH, RW, NW, NB}; KIND 0 ping-pongs the box
 // through shared memory (k_etb, NB buffer sets), KIND 1 keeps the bands in
 // registers (k_etbr, one staging set). The first shape of a depth is its
@@ -790,6 +988,113 @@ cudaError_t prepare_sweep_etb(TileConf &tc, int n) {
         return prepare_variant<K, D, CH, RW, NW, NB, MB>(tc, n);
         TBJ_ETB_VARIANTS(TBJ_PREP)
 #undef TBJ_PREP
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+bool etb_persistent_ok(const TileConf &tc) {
+    return tc.variant >= 0 &&
+           tc.variant < (int)(sizeof(kVariants) / sizeof(kVariants[0])) &&
+           kVariants[tc.variant].kind == 1;
+}
+
+namespace {
+
+template <int D, int CH, int RW, int NW, int MB>
+cudaError_t prepare_persistent(TileConf &tc, int n) {
+    using S = EtbrShape<D, CH, RW, NW>;
+    const void *kernels[2] = {(const void *)k_etbp<D, CH, RW, NW, MB, true>,
+                              (const void *)k_etbp<D, CH, RW, NW, MB, false>};
+    for (const void *k : kernels) {
+        cudaError_t e = cudaFuncSetAttribute(
+            k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+        if (e != cudaSuccess) return e;
+    }
+    // Every block must be resident at once (grid barriers): as many as fit,
+    // at most one per tile.
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, k_etbp<D, CH, RW, NW, MB, true>, 32 * NW, S::SMEM);
+    if (e == cudaSuccess) {
+        int per_sm2 = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm2, k_etbp<D, CH, RW, NW, MB, false>, 32 * NW, S::SMEM);
+        if (per_sm2 < per_sm) per_sm = per_sm2;
+    }
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int tiles = ((n - 1 + S::TX - 1) / S::TX) * ((n - 1 + S::TY - 1) / S::TY);
+    tc.ctas = sms * per_sm < tiles ? sms * per_sm : tiles;
+    tc.smem = S::SMEM;
+    return cudaSuccess;
+}
+
+template <int D, int CH, int RW, int NW, int MB>
+cudaError_t launch_persistent(const GridDesc &g, const TileConf &tc,
+                              const CUtensorMap *map_u,
+                              const CUtensorMap *map_alt,
+                              const CUtensorMap *map_b, float *u, float *u_alt,
+                              const LoopParams &lp, int rounds_per_check,
+                              cudaStream_t stream) {
+    using S = EtbrShape<D, CH, RW, NW>;
+    const int tiles_x = (g.n - 1 + S::TX - 1) / S::TX;
+    const int tiles = tiles_x * ((g.n - 1 + S::TY - 1) / S::TY);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tc.ctas);
+    cfg.blockDim = dim3(32 * NW);
+    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (g.fast)
+        return cudaLaunchKernelEx(&cfg, k_etbp<D, CH, RW, NW, MB, true>, *map_u,
+                                  *map_alt, *map_b, u, u_alt, g.n, g.ld, g.r,
+                                  g.d, g.y, lp, rounds_per_check, tiles_x, tiles);
+    return cudaLaunchKernelEx(&cfg, k_etbp<D, CH, RW, NW, MB, false>, *map_u,
+                              *map_alt, *map_b, u, u_alt, g.n, g.ld, g.r, g.d,
+                              g.y, lp, rounds_per_check, tiles_x, tiles);
+}
+
+}  // namespace
+
+cudaError_t prepare_etb_persistent(TileConf &tc, int n) {
+    switch (tc.variant) {
+#define TBJ_PPREP(I, K, D, CH, RW, NW, NB, MB)                           \
+    case I:                                                              \
+        if constexpr (K == 1) return prepare_persistent<D, CH, RW, NW, MB>(tc, n); \
+        return cudaErrorInvalidValue;
+        TBJ_ETB_VARIANTS(TBJ_PPREP)
+#undef TBJ_PPREP
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_etb_persistent(const GridDesc &g, const TileConf &tc,
+                                  const CUtensorMap *map_u,
+                                  const CUtensorMap *map_alt,
+                                  const CUtensorMap *map_b, float *u,
+                                  float *u_alt, const LoopParams &lp,
+                                  long long rounds_per_check,
+                                  cudaStream_t stream) {
+    switch (tc.variant) {
+#define TBJ_PLAUNCH(I, K, D, CH, RW, NW, NB, MB)                          \
+    case I:                                                               \
+        if constexpr (K == 1)                                             \
+            return launch_persistent<D, CH, RW, NW, MB>(                  \
+                g, tc, map_u, map_alt, map_b, u, u_alt, lp,               \
+                (int)rounds_per_check, stream);                           \
+        return cudaErrorInvalidValue;
+        TBJ_ETB_VARIANTS(TBJ_PLAUNCH)
+#undef TBJ_PLAUNCH
         default:
             return cudaErrorInvalidValue;
     }

@@ -333,6 +333,8 @@ __global__ void k_loop_reset(LoopState *st, const LoopState *prev) {
     st->status = 0;
     st->where = 0;
     st->rbits = 0u;
+    st->bar_arrive = 0u;
+    st->bar_epoch = 0u;
     if (prev && prev->status != 0) {
         st->status = kStepSkipped;
         st->stop = 1;

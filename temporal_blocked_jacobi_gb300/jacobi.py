@@ -13,14 +13,15 @@ import threading
 from . import _build
 
 SYNC, EXACT_TEMPORAL_BLOCKED, BLOCK_ASYNC = 0, 1, 2
-CONTROL_HOST, CONTROL_DEVICE = 0, 1
+CONTROL_HOST, CONTROL_DEVICE, CONTROL_PERSISTENT = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_CUDA, ERR_NOT_CONVERGED, ERR_NONFINITE, \
     ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 
 STRATEGIES = {"sync": SYNC, "etb": EXACT_TEMPORAL_BLOCKED,
               "exact_temporal_blocked": EXACT_TEMPORAL_BLOCKED,
               "ba": BLOCK_ASYNC, "block_async": BLOCK_ASYNC}
-CONTROLS = {"host": CONTROL_HOST, "device": CONTROL_DEVICE}
+CONTROLS = {"host": CONTROL_HOST, "device": CONTROL_DEVICE,
+            "persistent": CONTROL_PERSISTENT}
 DIVISION_AUTO, DIVISION_IEEE = 0, 1
 DIVISIONS = {"auto": DIVISION_AUTO, "ieee": DIVISION_IEEE}
 RHS_FUSED, RHS_UNFUSED = 0, 1

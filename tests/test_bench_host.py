@@ -90,3 +90,10 @@ def test_kernel_names_follow_default_shapes():
     assert bench.kernel_name("ba8").startswith("k_bar")
     assert bench.kernel_name("ba8@32x16").startswith("k_ba ")
     assert bench.kernel_name("ba8o4").startswith("k_ba ")
+
+
+def test_persistent_token():
+    kw = bench.parse_strategy("etb8p")
+    assert kw["strategy"] == "etb" and kw["depth"] == 8
+    assert kw["control"] == "persistent"
+    assert bench.kernel_name("etb8p").startswith("k_etbp")
