@@ -45,3 +45,41 @@ def test_kernels_compiled_for_sm103a_without_fast_math():
     assert "arch=compute_103a,code=sm_103a" in flags
     assert "-fmad=false" in flags and "-ftz=false" in flags
     assert "use_fast_math" not in flags
+
+
+def header_enum_values():
+    """name -> value of every enumerator in include/jacobi.h."""
+    text = open(os.path.join(ROOT, "include", "jacobi.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    values = {}
+    for body in re.findall(r"typedef\s+enum\s*\{(.*?)\}", text, flags=re.S):
+        nxt = 0
+        for item in body.split(","):
+            item = item.strip()
+            if not item:
+                continue
+            m = re.match(r"(\w+)\s*(?:=\s*(-?\d+))?$", item)
+            assert m, item
+            nxt = int(m.group(2)) if m.group(2) is not None else nxt
+            values[m.group(1)] = nxt
+            nxt += 1
+    return values
+
+
+def test_binding_constants_match_the_header():
+    from temporal_blocked_jacobi_gb300 import jacobi
+    v = header_enum_values()
+    assert v["JACOBI_SYNC"] == jacobi.SYNC
+    assert v["JACOBI_EXACT_TEMPORAL_BLOCKED"] == jacobi.EXACT_TEMPORAL_BLOCKED
+    assert v["JACOBI_BLOCK_ASYNC"] == jacobi.BLOCK_ASYNC
+    assert v["JACOBI_CONTROL_HOST"] == jacobi.CONTROL_HOST
+    assert v["JACOBI_CONTROL_DEVICE"] == jacobi.CONTROL_DEVICE
+    assert v["JACOBI_CONTROL_PERSISTENT"] == jacobi.CONTROL_PERSISTENT
+    assert jacobi.CONTROLS == {"host": 0, "device": 1, "persistent": 2}
+    for name, val in (("JACOBI_OK", jacobi.OK),
+                      ("JACOBI_ERR_INVALID_ARG", jacobi.ERR_INVALID_ARG),
+                      ("JACOBI_ERR_CUDA", jacobi.ERR_CUDA),
+                      ("JACOBI_ERR_NOT_CONVERGED", jacobi.ERR_NOT_CONVERGED),
+                      ("JACOBI_ERR_NONFINITE", jacobi.ERR_NONFINITE),
+                      ("JACOBI_ERR_UNSUPPORTED", jacobi.ERR_UNSUPPORTED)):
+        assert v[name] == val, name
