@@ -116,6 +116,59 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def sm_max_mhz():
+    """Maximum SM clock: MEASURED_PEAKS.json's figure, else GB300's 2070 MHz."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["sm_max_mhz"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 2070.0, "nominal"
+
+
+# FP32 pipe operations one lattice update needs at least: the 5 of the update
+# (W+E, N+S, their sum, r*s, b + r*s) and the 3 of a correctly rounded
+# division by the fixed d (q0 = x*y, rho = fma(q0, d, -x), q = fma(-rho, y,
+# q0)). Each SM's FP32 pipe issues 128 of them per clock.
+FP32_OPS_PER_LUP = 8
+FP32_LANES_PER_SM = 128
+
+
+def roofline_record(kw, interior, launch_ms, working_set, l2_bytes, sms,
+                    hbm_peak, hbm_how, mhz, mhz_how):
+    """Roofline of one sweep launch of strategy `kw` taking launch_ms.
+
+    HBM view: the algorithmic bytes of a launch (12 B per interior point, 16
+    with the unfused right-hand side) over its duration, against the measured
+    copy bandwidth. ALU view: FP32_OPS_PER_LUP operations per lattice update
+    (D updates per point per launch) against 128 lanes x SMs x the SM clock.
+    When u, u_alt and b fit in L2 the launches of a solve do not go to HBM,
+    so the bound reported is the FP32 pipe ("alu"); otherwise it is HBM."""
+    per = sweeps_per_launch(kw)
+    sec = launch_ms * 1e-3
+    alg_bytes = bytes_per_point(kw) * interior
+    gbs = alg_bytes / sec / 1e9
+    lups = interior * per / sec
+    ops = FP32_OPS_PER_LUP * lups / 1e12
+    alu_peak = FP32_LANES_PER_SM * sms * mhz * 1e6 / 1e12
+    hbm = {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+           "peak_source": (f"{hbm_how} (MEASURED_PEAKS.json hbm_gbs)"
+                           if hbm_how == "measured" else hbm_how)}
+    alu = {"achieved": ops, "peak": alu_peak, "unit": "Top/s", "frac": ops / alu_peak,
+           "peak_source": (f"{FP32_LANES_PER_SM} FP32 lanes x {sms} SMs x {mhz:.0f} MHz "
+                           f"(maximum SM clock, {mhz_how})"),
+           "ops_per_lup": FP32_OPS_PER_LUP}
+    l2_resident = working_set < l2_bytes
+    bound = "alu" if l2_resident else "hbm"
+    main = alu if bound == "alu" else hbm
+    return {"bound": bound, "achieved": main["achieved"], "peak": main["peak"],
+            "unit": main["unit"], "frac": main["frac"], "peak_source": main["peak_source"],
+            "hbm": hbm, "alu": alu,
+            "working_set_bytes": working_set, "l2_bytes": l2_bytes,
+            "l2_resident": l2_resident, "alg_bytes_per_launch": alg_bytes,
+            "launch_us": launch_ms * 1e3, "sweeps_per_launch": per, "lups_per_s": lups}
+
+
 # ---------------------------------------------------------------------------
 # Multi-process plumbing (replicas): max of the elapsed time and sum of the
 # work over ranks. Works with any torch.distributed backend.
@@ -357,8 +410,8 @@ def headline(results):
 
 def kernel_roofline(solver, tok, u, u0, stream, interior, args):
     """Average duration of the strategy's sweep kernel, launched back to back
-    on the solver's stream (no checks), against the HBM roofline with the
-    algorithmic 12 B per interior point per launch."""
+    on the solver's stream (no checks), as a roofline record
+    (roofline_record) with the DRAM traffic of the committed ncu capture."""
     import torch
     kw = parse_strategy(tok)
     per = sweeps_per_launch(kw)
@@ -372,22 +425,21 @@ def kernel_roofline(solver, tok, u, u0, stream, interior, args):
     end.record(stream)
     end.synchronize()
     ms = start.elapsed_time(end) / launches
-    alg_bytes = bytes_per_point(kw) * interior
-    peak, how = measured_peaks()
-    achieved = alg_bytes / (ms * 1e-3) / 1e9
-    traffic = load_traffic(tok, args.workload)
-    # u, u_alt and b; when they fit in L2 the launches of a solve hit L2 and
-    # HBM is not what bounds the kernel (the traffic figure shows it)
-    working_set = 3 * u.numel() * 4
-    l2 = torch.cuda.get_device_properties(u.device).L2_cache_size
-    return {"bound": "hbm", "kernel": kernel_name(tok), "achieved": achieved,
-            "working_set_bytes": working_set, "l2_bytes": l2,
-            "l2_resident": working_set < l2,
-            "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "peak_source": f"{how} (MEASURED_PEAKS.json hbm_gbs)" if how == "measured" else how,
-            "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
-            "launch_us": ms * 1e3, "sweeps_per_launch": per,
-            "lups_per_s": interior * per / (ms * 1e-3)}
+    props = torch.cuda.get_device_properties(u.device)
+    hbm_peak, hbm_how = measured_peaks()
+    mhz, mhz_how = sm_max_mhz()
+    # u, u_alt and b
+    rec = roofline_record(kw, interior, ms, 3 * u.numel() * 4, props.L2_cache_size,
+                          props.multi_processor_count, hbm_peak, hbm_how, mhz, mhz_how)
+    rec["kernel"] = kernel_name(tok)
+    rec["traffic"] = load_traffic(tok, args.workload)
+    return rec
+
+
+# Tile sizes (with (0, 0), the default) of the register-resident shapes of
+# exact temporal blocking, per depth.
+ETBR_TILES = {4: ((0, 0), (120, 88), (120, 40)), 8: ((0, 0), (112, 80), (112, 92)),
+              16: ((0, 0), (96, 64), (96, 76))}
 
 
 def kernel_name(tok):
@@ -396,8 +448,8 @@ def kernel_name(tok):
         return "k_sweep_sync" + (" (unfused rhs)" if kw.get("rhs") == "unfused" else "")
     if kw["strategy"] == "etb":
         # default shapes: bands in registers for D = 4, 8 and 16, box in
-        # shared memory for D = 2
-        name = ("k_etbr" if kw["depth"] in (4, 8, 16) and kw.get("tile", (0, 0)) == (0, 0)
+        # shared memory for D = 2; explicit tiles of the band shapes likewise
+        name = ("k_etbr" if kw.get("tile", (0, 0)) in ETBR_TILES.get(kw["depth"], ())
                 else "k_etb")
         if kw.get("control") == "persistent":
             name = "k_etbp"  # the whole step in one cooperative launch

@@ -845,9 +845,16 @@ k_etbp(const __grid_constant__ CUtensorMap map_u,
 
 // Shapes per depth: {KIND, CH, RW, NW, NB}; KIND 0 ping-pongs the box
 // through shared memory (k_etb, NB buffer sets), KIND 1 keeps the bands in
-// registers (k_etbr, one staging set). The first shape of a depth is its
-// default (fastest measured on GB300); the others are selected by their exact
-// tile size, the first listed winning.
+// registers (k_etbr, one staging set). Without a tile size the default is
+// the register-resident one-block-per-SM shape that leaves each SM the
+// fewest box rows to sweep for this grid (etb_default_variant), else the
+// first shape of the depth; with one, the shape of that exact tile size, the
+// first listed winning. The 12-warp x 9-row boxes exist for their tile
+// counts: at N = 2048 a D = 8 launch needs 4 rounds of the 152 SMs with
+// 80-row tiles and 3 with 92-row ones (measured on GB300: 14.9 against
+// 16.3 ms per ten-step solve; D = 16: 14.1 against 14.8 ms). Taller bands
+// in fewer warps lose more per row than their tile count saves (8 warps x 13
+// rows: 17.2 ms), and 12 x 12 or 16 x 7 rows spill registers.
 struct EtbVariant {
     int depth, kind, ch, rw, nw, nb, minb;
 };
@@ -858,6 +865,7 @@ constexpr EtbVariant kVariants[] = {
     {8, 1, 1, 6, 16, 1, 1}, {8, 0, 1, 4, 16, 2, 1}, {8, 0, 1, 4, 32, 1, 1},
     {8, 0, 2, 4, 16, 1, 1},
     {16, 1, 1, 6, 16, 1, 1}, {16, 0, 1, 4, 32, 1, 1}, {16, 0, 2, 3, 32, 1, 1},
+    {8, 1, 1, 9, 12, 1, 1}, {16, 1, 1, 9, 12, 1, 1},
 };
 
 template <int K, int D, int CH, int RW, int NW, int NB, int MB, bool F,
@@ -944,14 +952,51 @@ cudaError_t prepare_variant(TileConf &tc, int n) {
     X(10, 0, 8, 2, 4, 16, 1, 1)    \
     X(11, 1, 16, 1, 6, 16, 1, 1)   \
     X(12, 0, 16, 1, 4, 32, 1, 1)   \
-    X(13, 0, 16, 2, 3, 32, 1, 1)
+    X(13, 0, 16, 2, 3, 32, 1, 1)   \
+    X(14, 1, 8, 1, 9, 12, 1, 1)    \
+    X(15, 1, 16, 1, 9, 12, 1, 1)
+
+}  // namespace
+
+namespace {
+
+// The default shape of a depth for an N x N grid: among the register-resident
+// shapes with one block per SM, the fewest box rows per SM,
+// ceil(tiles / SMs) x box height (the box is 128 columns wide for all of
+// them), the first listed winning ties. -1 when the depth has no such shape
+// or the SM count cannot be read.
+int etb_default_variant(int n, int depth) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        sms < 1) {
+        cudaGetLastError();
+        return -1;
+    }
+    int pick = -1;
+    long long best = 0;
+    for (int v = 0; v < (int)(sizeof(kVariants) / sizeof(kVariants[0])); ++v) {
+        const EtbVariant &k = kVariants[v];
+        if (k.depth != depth || k.kind != 1 || k.minb != 1 || k.ch != 1) continue;
+        const int hx = (depth + 3) / 4 * 4;
+        const int by = k.nw * k.rw;
+        const long long tx = 128 - 2 * hx, ty = by - 2 * depth;
+        const long long tiles = ((n - 1 + tx - 1) / tx) * ((n - 1 + ty - 1) / ty);
+        const long long rows = (tiles + sms - 1) / sms * by;
+        if (pick < 0 || rows < best) {
+            pick = v;
+            best = rows;
+        }
+    }
+    return pick;
+}
 
 }  // namespace
 
 int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
-    (void)n;
     if (depth != 2 && depth != 4 && depth != 8 && depth != 16) return -1;
-    int pick = -1;
+    int pick = tile_x == 0 && tile_y == 0 ? etb_default_variant(n, depth) : -1;
     for (int v = 0; v < (int)(sizeof(kVariants) / sizeof(kVariants[0])); ++v) {
         const EtbVariant &k = kVariants[v];
         if (k.depth != depth) continue;

@@ -87,6 +87,8 @@ def test_kernel_names_follow_default_shapes():
     assert bench.kernel_name("etb4").startswith("k_etbr")
     assert bench.kernel_name("etb2").startswith("k_etb ")
     assert bench.kernel_name("etb8@112x48").startswith("k_etb ")
+    assert bench.kernel_name("etb8@112x92").startswith("k_etbr")
+    assert bench.kernel_name("etb16@96x64").startswith("k_etbr")
     assert bench.kernel_name("ba8").startswith("k_bar")
     assert bench.kernel_name("ba8@32x16").startswith("k_ba ")
     assert bench.kernel_name("ba8o4").startswith("k_ba ")
@@ -97,3 +99,26 @@ def test_persistent_token():
     assert kw["strategy"] == "etb" and kw["depth"] == 8
     assert kw["control"] == "persistent"
     assert bench.kernel_name("etb8p").startswith("k_etbp")
+
+
+def test_roofline_bound_follows_l2_residency():
+    """In L2 the sweep launches do not reach HBM: the record takes the FP32
+    pipe as the bound (8 operations per lattice update against 128 lanes x
+    SMs x clock); out of L2 it takes the measured HBM copy bandwidth with the
+    algorithmic 12 B per point per launch."""
+    kw = bench.parse_strategy("etb8")
+    interior = 2046 ** 2
+    args = (kw, interior, 0.027, 50_331_648)
+    rest = (152, 6774.9, "measured", 2070.0, "measured")
+    in_l2 = bench.roofline_record(*args, 132_120_576, *rest)
+    assert in_l2["bound"] == "alu" and in_l2["l2_resident"]
+    assert in_l2["peak"] == pytest.approx(128 * 152 * 2070e6 / 1e12)
+    assert in_l2["achieved"] == pytest.approx(8 * interior * 8 / 0.027e-3 / 1e12)
+    assert in_l2["frac"] == pytest.approx(in_l2["achieved"] / in_l2["peak"])
+    assert in_l2["hbm"]["achieved"] == pytest.approx(12 * interior / 0.027e-3 / 1e9)
+    out = bench.roofline_record(*args, 40_000_000, *rest)
+    assert out["bound"] == "hbm" and out["unit"] == "GB/s"
+    assert out["frac"] == pytest.approx(out["hbm"]["achieved"] / 6774.9)
+    unfused = bench.roofline_record(bench.parse_strategy("syncu"), interior, 0.027,
+                                    50_331_648, 40_000_000, *rest)
+    assert unfused["alg_bytes_per_launch"] == 16 * interior

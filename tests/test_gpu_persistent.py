@@ -31,6 +31,19 @@ def test_persistent_run_bit_exact(n, depth):
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
 
 
+@pytest.mark.parametrize("depth,tile", [(4, (120, 88)), (8, (112, 80)), (8, (112, 92)),
+                                        (16, (96, 64)), (16, (96, 76))])
+def test_persistent_register_shapes_bit_exact(depth, tile):
+    """Every register-resident tile shape, selected by its size, on a grid of
+    many ragged tiles."""
+    u0, g = workload(300, "gauss")
+    ref_u, ref_k, _ = oracle.run(u0, g, 10.0, steps=2, m=max(8, depth))
+    got_u, got_k, _ = gpu_run(u0, g, 10.0, steps=2, strategy="etb", depth=depth,
+                              tile=tile, control="persistent")
+    assert got_k == ref_k
+    assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
+
+
 @pytest.mark.parametrize("depth", [4, 8])
 def test_persistent_n2048_r10_gauss_bit_exact(depth):
     u0, g = workload(2048, "gauss")

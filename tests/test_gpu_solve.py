@@ -51,11 +51,12 @@ def test_n2048_r10_gauss_bit_exact(n2048_reference, strategy, depth, control):
     assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
 
 
-# Non-default compiled tile shapes of exact temporal blocking (the defaults
-# run in the N = 2048 test above).
+# Every compiled tile shape of exact temporal blocking, selected by its tile
+# size (the defaults depend on N; those of N = 2048 run in the test above).
 ETB_SHAPES = [(2, (120, 60)), (2, (248, 60)), (4, (120, 56)), (4, (248, 56)),
-              (4, (120, 40)), (8, (112, 48)), (8, (112, 112)), (8, (240, 48)),
-              (16, (96, 96)), (16, (224, 64))]
+              (4, (120, 40)), (8, (112, 80)), (8, (112, 48)), (8, (112, 112)),
+              (8, (240, 48)), (8, (112, 92)), (16, (96, 64)), (16, (96, 96)),
+              (16, (224, 64)), (16, (96, 76))]
 
 
 @pytest.mark.parametrize("depth,tile", ETB_SHAPES)
