@@ -138,7 +138,12 @@ typedef struct {
     int depth;            /* D: SYNC 1; EXACT_TEMPORAL_BLOCKED 2,4,8,16; BLOCK_ASYNC 1,2,4,8,16,32 */
     int tile_x, tile_y;   /* tile shape in cells; 0 = library default for the strategy.
                              tile_x a multiple of 4 for both tiled strategies;
-                             BLOCK_ASYNC default 32 x 8 (section 02) */
+                             BLOCK_ASYNC default 32 x 8 (section 02).
+                             EXACT_TEMPORAL_BLOCKED defaults depend on n: the
+                             register-resident shape that leaves each SM the
+                             fewest box rows (D = 4: 120 x 88; D = 8: 112 x 80
+                             or 112 x 92; D = 16: 96 x 64 or 96 x 76); D = 2:
+                             120 x 92. Any shape gives the same bits. */
     int check_every;      /* M: residual checked every lcm(M, sweeps per launch) sweeps; default 8 */
     double tol;           /* stop when rmax < tol * bmax (or rmax == 0); default 1e-5 */
     long long max_sweeps; /* give up (JACOBI_ERR_NOT_CONVERGED) at this many sweeps; default 1<<22 */
