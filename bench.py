@@ -3,25 +3,35 @@
 
 One bench step = one full run of the method on one synthetic workload: u⁰
 reset, then ten backward-Euler time steps (fused right-hand side, Jacobi
-sweeps of the chosen strategy, residual every check interval, host stop
+sweeps of the chosen strategy, residual every check interval, stop
 decision), timed with CUDA events on the solver's stream, checks included
 ("Synchronous vs block-async Jacobi on one RTX 5050", sections 01-03).
 
-Default workload: N = 2048 (ring included), r = 10, Gaussian source
-σ = N/16, amplitude 100, 10 time steps, tol 1e-5, M = 8; strategies SYNC and
-EXACT_TEMPORAL_BLOCKED with D = 2, 4, 8; convergence loop on the device
-(--control host: one host round trip per check instead). `value` is the GLUP/s (interior
-points × sweeps ÷ time) of the strategy with the shortest ten-step
-time-to-solution; every strategy's figures are under "strategies". SYNC and
+Default workload: the largest grid, N = 18432 (ring included; 1.36 GB per
+field, far beyond L2), r = 10, point source 1000 at the centre, 10 time
+steps, tol 1e-5, M = 8; strategies SYNC, EXACT_TEMPORAL_BLOCKED D = 8 and
+BLOCK_ASYNC D = 8; convergence loop on the device (--control host: one host
+round trip per check instead). `value` is the GLUP/s (interior points ×
+sweeps ÷ time) of the strategy with the shortest ten-step time-to-solution;
+every strategy's figures are under "strategies". SYNC and
 EXACT_TEMPORAL_BLOCKED perform the same sweeps (exact temporal blocking is
-bit-identical to SYNC), so their GLUP/s compare time-to-solution directly;
-BLOCK_ASYNC needs s times the sweeps and its GLUP/s counts them.
+bit-identical to SYNC, which the line re-checks on the final fields), so
+their GLUP/s compare time-to-solution directly; BLOCK_ASYNC needs s times
+the sweeps, its GLUP/s counts them, and its final field is checked against
+the SYNC field within 5e-4 ||b||inf.
+
+Besides the headline kernel's roofline the line carries the synchronous
+sweep's HBM roofline on the same grid ("roofline_sync") and at N = 8192
+("roofline_sync_n8192").
 
 Usage:
   python bench.py [--steps K] [--warmup W] [--workload NAME]
-                  [--strategies sync,etb2,etb4,etb8] [--impl ours|reference]
-Multi-GPU (torchrun, one rank per GPU): independent replicas of the same
-solve, no data exchange; value = all ranks' lattice updates ÷ max time.
+                  [--strategies sync,etb8,ba8] [--impl ours|reference]
+                  [--gpus N]
+Multi-GPU: independent replicas of the same solve, one process per GPU, no
+data exchange; value = all ranks' lattice updates ÷ max time. Under torchrun
+the ranks come from the environment; with --gpus N > 1 and no torchrun
+environment bench.py starts the N ranks itself through torch.distributed.run.
 """
 from __future__ import annotations
 
@@ -56,7 +66,7 @@ WORKLOADS = {
     "n4096_r100_gauss": (4096, 100.0, "gauss",
                          "sync,syncu,etb2,etb4,etb8,etb16,ba2,ba4,ba8,ba16,gasc8,gdesc8,gfb8"),
 }
-DEFAULT_WORKLOAD = "n2048_r10_gauss"
+DEFAULT_WORKLOAD = "n18432_r10_point"
 TIME_STEPS = 10
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
@@ -193,6 +203,13 @@ def aggregate(local_units: float, local_seconds: float, device=None):
     return float(t.item()), float(s.item())
 
 
+def replica_glups(local_lups: float, local_seconds: float, device=None):
+    """Whole-job GLUP/s of independent replicas: every rank's lattice
+    updates over the slowest rank's time."""
+    units, seconds = aggregate(local_lups, local_seconds, device=device)
+    return units / seconds / 1e9
+
+
 def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -272,7 +289,7 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        dist.init_process_group(args.dist_backend)
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     n, r, source, default_strats = WORKLOADS[args.workload]
@@ -312,7 +329,6 @@ def run_ours(args):
             end.synchronize()
             return start.elapsed_time(end), counts, s.launch_count - l0
 
-        # warm-up (also checks that every strategy reaches the same answer)
         for tok in strategies:
             for _ in range(args.warmup):
                 one_step(tok)
@@ -329,6 +345,7 @@ def run_ours(args):
                     launches += nl
                 sweeps = sum(counts)
                 ms_med = statistics.median(times)
+                kw = parse_strategy(tok)
                 results[tok] = dict(
                     sweeps=sweeps, sweeps_per_step=counts,
                     ms_per_solve_median=ms_med, ms_per_solve_mean=sum(times) / len(times),
@@ -336,13 +353,16 @@ def run_ours(args):
                     glups=interior * sweeps / (ms_med * 1e-3) / 1e9,
                     sync_equiv_gbs=12.0 * interior * sweeps / (ms_med * 1e-3) / 1e9,
                     # (D varies under a depth controller: not defined there)
-                    alg_gbs=None if parse_strategy(tok).get("adapt") else
-                    bytes_per_point(parse_strategy(tok)) * interior * sweeps
-                    / sweeps_per_launch(parse_strategy(tok)) / (ms_med * 1e-3) / 1e9,
+                    alg_gbs=None if kw.get("adapt") else
+                    bytes_per_point(kw) * interior * sweeps
+                    / sweeps_per_launch(kw) / (ms_med * 1e-3) / 1e9,
                     launches=launches, total_ms=sum(times))
         torch.cuda.synchronize(dev)
         barrier()
         wall = time.perf_counter() - t_wall0
+
+        # --- after the timed region: the answers of the strategies
+        checks = answer_checks(solvers, strategies, u, u0, g, stream, n)
 
     best = headline(results)
     base = results.get("sync")
@@ -352,25 +372,36 @@ def run_ours(args):
             res["sweep_ratio_s"] = res["sweeps"] / base["sweeps"]
             # cost per sweep relative to a synchronous sweep: S = 1/(c*s)
             res["cost_per_sweep_c"] = 1.0 / (res["speedup_vs_sync"] * res["sweep_ratio_s"])
+        if tok in checks:
+            res["answer_check"] = checks[tok]
     if base and "syncu" in results:
         # section 05, Table VI: T_unfused / T_fused of the synchronous sweep
         results["syncu"]["t_unfused_over_fused"] = (
             results["syncu"]["ms_per_solve_median"] / base["ms_per_solve_median"])
     total_ms = sum(res["total_ms"] for res in results.values())
     total_lups = sum(interior * res["sweeps"] * args.steps for res in results.values())
-    lups_all, seconds_max = aggregate(float(interior * results[best]["sweeps"] * args.steps),
-                                      results[best]["total_ms"] * 1e-3,
-                                      device=dev if world > 1 else None)
-    value = lups_all / seconds_max / 1e9
+    value = replica_glups(float(interior * results[best]["sweeps"] * args.steps),
+                          results[best]["total_ms"] * 1e-3,
+                          device=dev if world > 1 else None)
 
     # --- dominant kernel: the headline strategy's sweep kernel, timed alone
-    roof = kernel_roofline(solvers[best], best, u, u0, stream, interior, args)
+    roof = kernel_roofline(solvers[best], best, u, u0, stream, interior, args.workload)
+    roof_sync = None
+    if "sync" in solvers and best != "sync":
+        roof_sync = kernel_roofline(solvers["sync"], "sync", u, u0, stream, interior,
+                                    args.workload)
 
     # --- end to end through the public API with host buffers
     e2e = end_to_end(solvers[best], u, g, u0_host, g_host, stream, interior, args)
 
     for s in solvers.values():
         s.close()
+    del u, u_alt, b, g, u0, flush
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    roof_8192 = None
+    if n != SYNC_ROOFLINE_N and not args.no_sync_n8192:
+        roof_8192 = sync_roofline_at(SYNC_ROOFLINE_N, dev)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -392,6 +423,17 @@ def run_ours(args):
         "lups_all_strategies": total_lups,
         "strategies": results,
     }
+    if roof_sync is not None:
+        line["roofline_sync"] = roof_sync
+    if roof_8192 is not None:
+        line["roofline_sync_n8192"] = roof_8192
+    if base:
+        etbs = [t for t in results if parse_strategy(t)["strategy"] == "etb"]
+        if etbs:
+            fastest = min(etbs, key=lambda t: results[t]["ms_per_solve_median"])
+            line["etb_over_sync"] = {
+                "strategy": fastest,
+                "time_to_solution_ratio": results[fastest]["speedup_vs_sync"]}
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(args)
@@ -401,6 +443,74 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# The grid on which the synchronous sweep's HBM fraction is also reported
+# (section 05 "Results beyond L2": 805 MB per sweep, far beyond L2).
+SYNC_ROOFLINE_N = 8192
+
+
+def answer_checks(solvers, strategies, u, u0, g, stream, n):
+    """After the timed region, one more ten-step run of each strategy from u⁰:
+    EXACT_TEMPORAL_BLOCKED must give SYNC's sweep counts and field bit for
+    bit; BLOCK_ASYNC must lie within 5e-4 ||b||inf of SYNC's field, ||b||inf
+    being the norm of SYNC's last right-hand side (section 02). Compared on
+    the device. Without a SYNC strategy there is nothing to compare with."""
+    import torch
+    if "sync" not in solvers:
+        return {}
+    s = solvers["sync"]
+    u.copy_(u0)
+    sync_counts = s.run(g, TIME_STEPS)
+    _, bmax = s.residual()
+    ref = u.clone()
+    out = {}
+    for tok in strategies:
+        kw = parse_strategy(tok)
+        if tok == "sync":
+            continue
+        u.copy_(u0)
+        counts = solvers[tok].run(g, TIME_STEPS)
+        torch.cuda.current_stream().wait_stream(stream)
+        diff = (u[1:n - 1, 1:n - 1] - ref[1:n - 1, 1:n - 1]).abs().max().item()
+        rec = {"max_abs_diff_vs_sync": diff, "bmax": float(bmax)}
+        if kw["strategy"] in ("etb", "sync"):
+            same = bool(torch.equal(u.view(torch.int32), ref.view(torch.int32)))
+            rec.update(kind="bit-exact vs sync", same_counts=counts == sync_counts,
+                       bit_identical=same, ok=same and counts == sync_counts)
+        else:
+            bound = 5e-4 * float(bmax)
+            rec.update(kind="within 5e-4 ||b||inf of sync", bound=bound,
+                       diff_over_bmax=diff / float(bmax) if bmax else None,
+                       ok=diff <= bound)
+        out[tok] = rec
+    del ref
+    return out
+
+
+def sync_roofline_at(n, dev):
+    """The synchronous sweep's HBM roofline on an N x N Gaussian problem (r =
+    100), launched back to back on a fresh solver after the timed region."""
+    import torch
+
+    from temporal_blocked_jacobi_gb300 import jacobi
+    ld = P.padded_ld(n)
+    interior = (n - 2) ** 2
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        u0 = torch.from_numpy(P.initial_field(n, ld)).to(dev)
+        g = torch.from_numpy(P.source_term(n, ld, "gauss")).to(dev)
+        u, u_alt, b = jacobi.allocate(n, ld, device=dev)
+        u.copy_(u0)
+        with jacobi.Solver(u, u_alt, b, 100.0, stream=stream) as s:
+            s.rhs(g)
+            rec = kernel_roofline(s, "sync", u, u0, stream, interior,
+                                  f"n{n}_r100_gauss")
+    rec["workload"] = f"n{n}_r100_gauss"
+    del u0, g, u, u_alt, b
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return rec
+
+
 def headline(results):
     """The strategy with the shortest ten-step time-to-solution. Block-async
     strategies sweep more often than SYNC (sweep ratio s > 1), so their
@@ -408,10 +518,11 @@ def headline(results):
     return min(results, key=lambda t: results[t]["ms_per_solve_median"])
 
 
-def kernel_roofline(solver, tok, u, u0, stream, interior, args):
+def kernel_roofline(solver, tok, u, u0, stream, interior, workload):
     """Average duration of the strategy's sweep kernel, launched back to back
-    on the solver's stream (no checks), as a roofline record
-    (roofline_record) with the DRAM traffic of the committed ncu capture."""
+    on the solver's stream (no checks) and timed there with CUDA events, as a
+    roofline record (roofline_record) with the DRAM traffic of the committed
+    ncu capture."""
     import torch
     kw = parse_strategy(tok)
     per = sweeps_per_launch(kw)
@@ -432,7 +543,8 @@ def kernel_roofline(solver, tok, u, u0, stream, interior, args):
     rec = roofline_record(kw, interior, ms, 3 * u.numel() * 4, props.L2_cache_size,
                           props.multi_processor_count, hbm_peak, hbm_how, mhz, mhz_how)
     rec["kernel"] = kernel_name(tok)
-    rec["traffic"] = load_traffic(tok, args.workload)
+    rec["launches_timed"] = launches
+    rec["traffic"] = load_traffic(tok, workload)
     return rec
 
 
@@ -505,25 +617,37 @@ def end_to_end(solver, u, g, u0_host, g_host, stream, interior, args):
 # ---------------------------------------------------------------------------
 # CPU oracle legs (test infrastructure, timed as a reported baseline)
 # ---------------------------------------------------------------------------
+class OracleSample:
+    """The oracle (single-threaded C) timed on a bounded sample of the
+    ten-step solve: the first `sweeps` sweeps, right-hand sides and residual
+    checks included, continuing into later time steps as each one converges.
+    The inputs are built once, outside the timed calls."""
+
+    def __init__(self, n, r, source):
+        import oracle
+        self.oracle = oracle
+        self.n, self.r = n, r
+        self.u0 = P.initial_field(n)
+        self.g = P.source_term(n, kind=source)
+        oracle.rhs(self.u0[:3, :4].copy(), self.g[:3, :4].copy(), 3)  # load the library
+
+    def __call__(self, sample_sweeps):
+        oracle = self.oracle
+        u = self.u0.copy()
+        done, steps = 0, 0
+        t0 = time.perf_counter()
+        while done < sample_sweeps and steps < TIME_STEPS:
+            b = oracle.rhs(u, self.g)
+            k, _, _ = oracle.solve_step(u, b, self.r, max_sweeps=sample_sweeps - done)
+            done += (sample_sweeps - done) if k < 0 else k
+            steps += 1
+        dt = time.perf_counter() - t0
+        return (self.n - 2) ** 2 * done / dt / 1e9, dt, done
+
+
 def oracle_sample(n, r, source, sample_sweeps):
-    """Time the oracle (single-threaded C) on the first `sample_sweeps`
-    sweeps of the ten-step solve (right-hand sides and residual checks
-    included), continuing into later time steps as each one converges."""
-    import oracle
-    u0 = P.initial_field(n)
-    g = P.source_term(n, kind=source)
-    u = u0.copy()
-    oracle.solve_step(u, oracle.rhs(u, g), r, max_sweeps=8)  # warm the library
-    u = u0.copy()
-    done, steps = 0, 0
-    t0 = time.perf_counter()
-    while done < sample_sweeps and steps < TIME_STEPS:
-        b = oracle.rhs(u, g)
-        k, _, _ = oracle.solve_step(u, b, r, max_sweeps=sample_sweeps - done)
-        done += (sample_sweeps - done) if k < 0 else k
-        steps += 1
-    dt = time.perf_counter() - t0
-    return (n - 2) ** 2 * done / dt / 1e9, dt, done
+    """One timed oracle sample of `sample_sweeps` sweeps: (GLUP/s, s, sweeps)."""
+    return OracleSample(n, r, source)(sample_sweeps)
 
 
 def cpu_baseline(args):
@@ -542,13 +666,14 @@ def run_reference(args):
     if rank != 0:
         return
     n, r, source, _ = WORKLOADS[args.workload]
+    # about 1e9 lattice updates per bench step (at least one check interval)
     sweeps = args.cpu_sample_sweeps or max(8, int(8 * round(1.0e9 / (n - 2) ** 2 / 8)))
-    oracle_sample(n, r, source, 8)  # warm-up outside the count
+    sample = OracleSample(n, r, source)
     for _ in range(args.warmup):
-        oracle_sample(n, r, source, sweeps)
+        sample(sweeps)
     vals, secs = [], []
     for _ in range(args.steps):
-        v, dt, done = oracle_sample(n, r, source, sweeps)
+        v, dt, done = sample(sweeps)
         vals.append(v)
         secs.append(dt)
     value = statistics.median(vals)
@@ -560,13 +685,29 @@ def run_reference(args):
             "config": {"workload": args.workload, "n": n, "r": r, "source": source,
                        "strategy": "sync (oracle)", "parallelism": "single host core"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"first {sweeps} sweeps of the ten-step solve per bench step"},
+                             "sample": f"first {sweeps} sweeps of the ten-step solve per "
+                                       "bench step, single-threaded C oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def spawn_ranks(nproc, argv, script=None):
+    """Start `nproc` ranks of `script` (default: this file) through
+    torch.distributed.run on 127.0.0.1, one process per GPU, and return the
+    launcher's exit code. The ranks see WORLD_SIZE and do not spawn again."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={nproc}", "--master-addr=127.0.0.1",
+           f"--master-port={port}", script or os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
@@ -578,11 +719,23 @@ def main(argv=None):
     ap.add_argument("--control", default="device", choices=["device", "host"],
                     help="convergence loop on the device (one graph per time "
                          "step) or on the host (one round trip per check)")
+    ap.add_argument("--dist-backend", default="nccl",
+                    help="torch.distributed backend of the replicas' two scalar "
+                         "reductions")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sync-n8192", action="store_true",
+                    help="skip the extra synchronous-sweep roofline at N = 8192")
     ap.add_argument("--cpu-sample-sweeps", type=int, default=0)
     args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(args.gpus, argv))
+    world, _, _ = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -122,3 +122,38 @@ def test_roofline_bound_follows_l2_residency():
     unfused = bench.roofline_record(bench.parse_strategy("syncu"), interior, 0.027,
                                     50_331_648, 40_000_000, *rest)
     assert unfused["alg_bytes_per_launch"] == 16 * interior
+
+
+def test_spawned_replicas_aggregate_on_two_gloo_ranks(capfd):
+    """--gpus N without a torchrun environment starts N ranks itself
+    (bench.spawn_ranks); the ranks' work is summed and their time maxed."""
+    rc = bench.spawn_ranks(2, [], script=os.path.join(ROOT, "tests", "replica_rank.py"))
+    out = capfd.readouterr().out
+    assert rc == 0, out
+    lines = [json.loads(x) for x in out.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    # (1e9 + 2e9) updates over max(0.5, 1.5) s
+    assert lines[0]["n_gpus"] == 2 and lines[0]["value"] == pytest.approx(2.0)
+
+
+def test_gpus_flag_spawns_the_reference_arm_once():
+    """bench.py --gpus 2 outside torchrun runs two ranks; only rank 0 prints
+    the reference line, and it declares both GPUs."""
+    res = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+         "--gpus", "2", "--workload", "n512_r1_point", "--steps", "1",
+         "--warmup", "0", "--cpu-sample-sweeps", "8"],
+        capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert res.returncode == 0, res.stderr
+    lines = [json.loads(x) for x in res.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1 and lines[0]["impl"] == "reference"
+    assert lines[0]["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    res = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+         "--gpus", "2", "--workload", "n512_r1_point"],
+        capture_output=True, text=True, timeout=120, cwd=ROOT,
+        env={**os.environ, "WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert res.returncode != 0 and "WORLD_SIZE" in res.stderr
