@@ -36,6 +36,9 @@ Functions and what pins them (tests/test_oracle_pins.py):
                                           halo as the ring; mirror symmetry;
                                           fewer sweeps with overlap
   run            ten-step driver       -- pinned through the above
+  threads > 1    row-parallel sweeps   -- pinned: bit-identical to one thread
+                 and residuals            (tests/test_oracle_threads.py); one
+                                          thread stays the oracle of record
 """
 from __future__ import annotations
 
@@ -50,7 +53,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = [os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "oracle_body.h")]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _CFLAGS = ["-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared"]
+           "-fPIC", "-shared", "-pthread"]
 _lock = threading.Lock()
 _lib = None
 
@@ -62,7 +65,7 @@ def build(force: bool = False) -> str:
     if stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         cc = os.environ.get("CC", "gcc")
-        subprocess.check_call([cc, *_CFLAGS, "-o", tmp, _SRC[0], "-lm"])
+        subprocess.check_call([cc, *_CFLAGS, "-o", tmp, _SRC[0], "-lm", "-lpthread"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -101,9 +104,17 @@ def _load():
             f.argtypes = [c_int, c_ll, real, c_int, c_d, c_ll, c_int, c_int,
                           c_int, c_int, c_int, rp, rp, rp, preal, preal]
             f.restype = c_ll
+            f = getattr(lib, f"oracle_solve_step_mt_{sfx}")
+            f.argtypes = [c_int, c_ll, real, c_int, c_d, c_ll, c_int, c_int,
+                          c_int, c_int, c_int, rp, rp, rp, preal, preal, c_int]
+            f.restype = c_ll
             f = getattr(lib, f"oracle_run_{sfx}")
             f.argtypes = [c_int, c_ll, real, c_int, c_d, c_ll, c_int, c_int,
                           c_int, c_int, c_int, c_int, rp, rp, rp, rp, i64p]
+            f.restype = c_ll
+            f = getattr(lib, f"oracle_run_mt_{sfx}")
+            f.argtypes = [c_int, c_ll, real, c_int, c_d, c_ll, c_int, c_int,
+                          c_int, c_int, c_int, c_int, rp, rp, rp, rp, i64p, c_int]
             f.restype = c_ll
         _lib = lib
         return lib
@@ -157,7 +168,10 @@ def sweeps(u, b, r, count, n=None):
 
 
 def residual(u, b, r, n=None):
-    """(rmax, bmax): max of d·|J(u)−u| and max |b| over the interior."""
+    """(rmax, bmax) over the interior: rmax = max d·|J(u)−u| (the difference
+    form of |b − Au|), bmax = max |b_I|, where b_I = b + r·(the cell's
+    Dirichlet-ring neighbours) is the right-hand side of the system in the
+    unknowns."""
     ld = _check(u, b)
     n = u.shape[0] if n is None else n
     real = ctypes.c_float if u.dtype == np.float32 else ctypes.c_double
@@ -194,35 +208,49 @@ def ba_overlap_launch(u, b, r, tile_x, tile_y, overlap_x, overlap_y, depth,
 
 
 def solve_step(u, b, r, *, m=8, tol=1e-5, max_sweeps=1 << 22, depth=0,
-               tile_x=32, tile_y=8, overlap=(0, 0), n=None):
+               tile_x=32, tile_y=8, overlap=(0, 0), n=None, threads=1):
     """Solve one step in place from the warm start u. Returns
     (status_or_sweeps, rmax, bmax). depth 0 = synchronous sweeps; depth ≥ 1 =
     block-asynchronous launches on tile_x×tile_y tiles (overlapping by
-    `overlap` = (ox, oy) cells when not zero)."""
+    `overlap` = (ox, oy) cells when not zero). threads > 1 splits the rows of
+    each synchronous sweep and residual among POSIX threads (same bits; the
+    single-threaded form is the oracle of record)."""
     ld = _check(u, b)
     n = u.shape[0] if n is None else n
     work = u.copy()
     real = ctypes.c_float if u.dtype == np.float32 else ctypes.c_double
     rm, bm = real(), real()
-    k = getattr(_load(), f"oracle_solve_step_{_sfx(u)}")(
-        n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
-        overlap[0], overlap[1], u, work, b, ctypes.byref(rm), ctypes.byref(bm))
+    if threads <= 1:
+        k = getattr(_load(), f"oracle_solve_step_{_sfx(u)}")(
+            n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
+            overlap[0], overlap[1], u, work, b, ctypes.byref(rm), ctypes.byref(bm))
+    else:
+        k = getattr(_load(), f"oracle_solve_step_mt_{_sfx(u)}")(
+            n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
+            overlap[0], overlap[1], u, work, b, ctypes.byref(rm), ctypes.byref(bm),
+            int(threads))
     return int(k), _real(u)(rm.value), _real(u)(bm.value)
 
 
 def run(u0, g, r, *, steps=10, m=8, tol=1e-5, max_sweeps=1 << 22, depth=0,
-        tile_x=32, tile_y=8, overlap=(0, 0), n=None):
+        tile_x=32, tile_y=8, overlap=(0, 0), n=None, threads=1):
     """Run `steps` backward-Euler steps from u⁰. Returns (u_final, sweeps per
-    step as a list, b of the last step). Raises on a negative status."""
+    step as a list, b of the last step). Raises on a negative status.
+    threads > 1: row-parallel synchronous sweeps and residuals (same bits)."""
     ld = _check(u0, g)
     n = u0.shape[0] if n is None else n
     u = u0.copy()
     work = u0.copy()
     b = np.zeros_like(u0)
     counts = np.zeros(steps, dtype=np.int64)
-    rc = getattr(_load(), f"oracle_run_{_sfx(u)}")(
-        n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
-        overlap[0], overlap[1], steps, u, g, work, b, counts)
+    if threads <= 1:
+        rc = getattr(_load(), f"oracle_run_{_sfx(u)}")(
+            n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
+            overlap[0], overlap[1], steps, u, g, work, b, counts)
+    else:
+        rc = getattr(_load(), f"oracle_run_mt_{_sfx(u)}")(
+            n, ld, _real(u)(r), m, tol, max_sweeps, depth, tile_x, tile_y,
+            overlap[0], overlap[1], steps, u, g, work, b, counts, int(threads))
     if rc < 0:
         raise RuntimeError(f"oracle run failed with status {rc}: {counts.tolist()}")
     return u, counts.tolist(), b

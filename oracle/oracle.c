@@ -10,11 +10,15 @@
  * (stencil-jacobian.vercel.app), sections 01 "The problem" and 02 "Method".
  *
  * Build: cc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared
- * (no multiply-add contraction, IEEE subnormals kept; see oracle/__init__.py).
+ * -pthread (no multiply-add contraction, IEEE subnormals kept; see
+ * oracle/__init__.py). The single-threaded functions are the oracle of
+ * record; the *_mt forms split a sweep's rows among POSIX threads and give
+ * the same bits (checked in tests/test_oracle_threads.py).
  *
  * Parity status of each function is recorded in oracle/__init__.py's header.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdlib.h>
 #include <string.h>
 

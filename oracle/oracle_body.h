@@ -58,17 +58,23 @@ void FN(oracle_rhs)(int n, long long ld, const REAL *u, const REAL *g,
         }
 }
 
-/* One synchronous sweep u -> out over all interior cells. The ring of out is
- * not written: the caller keeps both buffers' rings equal. */
-void FN(oracle_sweep)(int n, long long ld, REAL r, const REAL *u,
-                      const REAL *b, REAL *out) {
+/* Rows i0 <= i < i1 (interior rows only) of one synchronous sweep. */
+static void FN(sweep_rows)(int n, long long ld, REAL r, const REAL *u,
+                           const REAL *b, REAL *out, int i0, int i1) {
     REAL d = FN(diag)(r);
-    for (int i = 1; i < n - 1; ++i)
+    for (int i = i0; i < i1; ++i)
         for (int j = 1; j < n - 1; ++j) {
             long long p = (long long)i * ld + j;
             out[p] = FN(jacobi_point)(u[p - 1], u[p + 1], u[p - ld],
                                       u[p + ld], b[p], r, d);
         }
+}
+
+/* One synchronous sweep u -> out over all interior cells. The ring of out is
+ * not written: the caller keeps both buffers' rings equal. */
+void FN(oracle_sweep)(int n, long long ld, REAL r, const REAL *u,
+                      const REAL *b, REAL *out) {
+    FN(sweep_rows)(n, ld, r, u, b, out, 1, n - 1);
 }
 
 /* Is cell (i, j) on the Dirichlet ring? */
@@ -94,12 +100,18 @@ static int FN(on_ring)(int n, int i, int j) {
  * rmax = max e_ij, bmax = max |bI_ij| over the interior. A NaN anywhere makes
  * the corresponding norm NaN.
  */
-void FN(oracle_residual)(int n, long long ld, REAL r, const REAL *u,
-                         const REAL *b, REAL *rmax_out, REAL *bmax_out) {
+/* Partial norms over rows i0 <= i < i1: the largest non-NaN e and |bI| seen
+ * (from 0) and whether a NaN was seen. The maximum of a set does not depend
+ * on the order it is taken in, so partials over any split of the rows combine
+ * (max of the maxima, OR of the flags) to exactly the whole-grid result. */
+static void FN(residual_rows)(int n, long long ld, REAL r, const REAL *u,
+                              const REAL *b, int i0, int i1, REAL *rmax_out,
+                              REAL *bmax_out, int *r_nan_out,
+                              int *b_nan_out) {
     REAL d = FN(diag)(r);
     REAL rmax = 0, bmax = 0;
     int r_nan = 0, b_nan = 0;
-    for (int i = 1; i < n - 1; ++i)
+    for (int i = i0; i < i1; ++i)
         for (int j = 1; j < n - 1; ++j) {
             long long p = (long long)i * ld + j;
             REAL ju = FN(jacobi_point)(u[p - 1], u[p + 1], u[p - ld],
@@ -119,8 +131,115 @@ void FN(oracle_residual)(int n, long long ld, REAL r, const REAL *u,
             if (bb != bb) b_nan = 1;
             else if (bb > bmax) bmax = bb;
         }
+    *rmax_out = rmax;
+    *bmax_out = bmax;
+    *r_nan_out = r_nan;
+    *b_nan_out = b_nan;
+}
+
+void FN(oracle_residual)(int n, long long ld, REAL r, const REAL *u,
+                         const REAL *b, REAL *rmax_out, REAL *bmax_out) {
+    REAL rmax, bmax;
+    int r_nan, b_nan;
+    FN(residual_rows)(n, ld, r, u, b, 1, n - 1, &rmax, &bmax, &r_nan, &b_nan);
     *rmax_out = r_nan ? (REAL)NAN : rmax;
     *bmax_out = b_nan ? (REAL)NAN : bmax;
+}
+
+/*
+ * Row-parallel forms of the sweep and the residual, for checking large grids
+ * in reasonable time. Every cell is computed by the same code as above, and a
+ * sweep's cells are independent of each other (Jacobi reads only the previous
+ * iterate), so splitting the interior rows among threads gives the same bits
+ * as one thread; the residual's partial maxima combine exactly (see
+ * residual_rows). threads <= 1 calls the single-threaded functions.
+ */
+typedef struct {
+    int kind; /* 0 sweep, 1 residual */
+    int n;
+    long long ld;
+    REAL r;
+    const REAL *u, *b;
+    REAL *out;
+    int i0, i1;
+    REAL rmax, bmax;
+    int r_nan, b_nan;
+} FN(rows_job);
+
+static void *FN(rows_worker)(void *arg) {
+    FN(rows_job) *j = (FN(rows_job) *)arg;
+    if (j->kind == 0)
+        FN(sweep_rows)(j->n, j->ld, j->r, j->u, j->b, j->out, j->i0, j->i1);
+    else
+        FN(residual_rows)(j->n, j->ld, j->r, j->u, j->b, j->i0, j->i1,
+                          &j->rmax, &j->bmax, &j->r_nan, &j->b_nan);
+    return NULL;
+}
+
+#define ORACLE_MAX_THREADS 256
+
+/* Run `proto` over the interior rows split into `threads` contiguous ranges
+ * (job 0 on the calling thread). Returns 0, or -2 if a thread could not be
+ * started (all started threads are joined first). */
+static int FN(run_rows)(int threads, const FN(rows_job) *proto,
+                        FN(rows_job) *jobs) {
+    int rows = proto->n - 2;
+    if (threads > rows) threads = rows;
+    if (threads < 1) threads = 1;
+    pthread_t tid[ORACLE_MAX_THREADS];
+    int started[ORACLE_MAX_THREADS];
+    int rc = 0;
+    for (int t = 0; t < threads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].i0 = 1 + (int)((long long)rows * t / threads);
+        jobs[t].i1 = 1 + (int)((long long)rows * (t + 1) / threads);
+        started[t] = 0;
+    }
+    for (int t = 1; t < threads; ++t) {
+        if (pthread_create(&tid[t], NULL, FN(rows_worker), &jobs[t]) == 0)
+            started[t] = 1;
+        else
+            rc = -2;
+    }
+    if (rc == 0) FN(rows_worker)(&jobs[0]);
+    for (int t = 1; t < threads; ++t)
+        if (started[t]) pthread_join(tid[t], NULL);
+    return rc;
+}
+
+static int FN(sweep_mt)(int threads, int n, long long ld, REAL r,
+                        const REAL *u, const REAL *b, REAL *out) {
+    if (threads <= 1) {
+        FN(oracle_sweep)(n, ld, r, u, b, out);
+        return 0;
+    }
+    FN(rows_job) proto = {0, n, ld, r, u, b, out, 0, 0, 0, 0, 0, 0};
+    FN(rows_job) jobs[ORACLE_MAX_THREADS];
+    return FN(run_rows)(threads, &proto, jobs);
+}
+
+static int FN(residual_mt)(int threads, int n, long long ld, REAL r,
+                           const REAL *u, const REAL *b, REAL *rmax_out,
+                           REAL *bmax_out) {
+    if (threads <= 1) {
+        FN(oracle_residual)(n, ld, r, u, b, rmax_out, bmax_out);
+        return 0;
+    }
+    FN(rows_job) proto = {1, n, ld, r, u, b, NULL, 0, 0, 0, 0, 0, 0};
+    FN(rows_job) jobs[ORACLE_MAX_THREADS];
+    int nt = threads > n - 2 ? n - 2 : threads;
+    if (FN(run_rows)(threads, &proto, jobs)) return -2;
+    REAL rmax = 0, bmax = 0;
+    int r_nan = 0, b_nan = 0;
+    for (int t = 0; t < nt; ++t) {
+        r_nan |= jobs[t].r_nan;
+        b_nan |= jobs[t].b_nan;
+        if (jobs[t].rmax > rmax) rmax = jobs[t].rmax;
+        if (jobs[t].bmax > bmax) bmax = jobs[t].bmax;
+    }
+    *rmax_out = r_nan ? (REAL)NAN : rmax;
+    *bmax_out = b_nan ? (REAL)NAN : bmax;
+    return 0;
 }
 
 /*
@@ -292,12 +411,14 @@ static long long FN(gcd)(long long a, long long b) {
  * -3 when max_sweeps is reached without convergence, -4 on non-finite norms,
  * -1 on bad arguments.
  */
-long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
-                                double tol, long long max_sweeps, int depth,
-                                int tx, int ty, int ox, int oy, REAL *u,
-                                REAL *work, const REAL *b, REAL *rmax_out,
-                                REAL *bmax_out) {
+long long FN(oracle_solve_step_mt)(int n, long long ld, REAL r, int m,
+                                   double tol, long long max_sweeps,
+                                   int depth, int tx, int ty, int ox, int oy,
+                                   REAL *u, REAL *work, const REAL *b,
+                                   REAL *rmax_out, REAL *bmax_out,
+                                   int threads) {
     if (n < 3 || ld < n || m < 1 || depth < 0) return -1;
+    if (threads > ORACLE_MAX_THREADS) threads = ORACLE_MAX_THREADS;
     long long per_launch = depth == 0 ? 1 : depth;
     long long interval = (long long)m / FN(gcd)(m, per_launch) * per_launch;
     long long launches_per_check = interval / per_launch;
@@ -307,9 +428,9 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
     REAL rmax = 0, bmax = 0;
     for (;;) {
         for (long long l = 0; l < launches_per_check; ++l) {
-            if (depth == 0)
-                FN(oracle_sweep)(n, ld, r, cur, b, nxt);
-            else if (ox == 0 && oy == 0) {
+            if (depth == 0) {
+                if (FN(sweep_mt)(threads, n, ld, r, cur, b, nxt)) return -2;
+            } else if (ox == 0 && oy == 0) {
                 if (FN(oracle_ba_launch)(n, ld, r, tx, ty, depth, cur, b, nxt))
                     return -1;
             } else if (FN(oracle_ba_overlap_launch)(n, ld, r, tx, ty, ox, oy,
@@ -318,7 +439,7 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
             REAL *t = cur; cur = nxt; nxt = t;
         }
         k += interval;
-        FN(oracle_residual)(n, ld, r, cur, b, &rmax, &bmax);
+        if (FN(residual_mt)(threads, n, ld, r, cur, b, &rmax, &bmax)) return -2;
         int c = FN(converged)(rmax, bmax, tol);
         if (c < 0) { status = -4; break; }
         if (c > 0) { status = k; break; }
@@ -330,6 +451,17 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
     return status;
 }
 
+/* The oracle of record: one thread. */
+long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
+                                double tol, long long max_sweeps, int depth,
+                                int tx, int ty, int ox, int oy, REAL *u,
+                                REAL *work, const REAL *b, REAL *rmax_out,
+                                REAL *bmax_out) {
+    return FN(oracle_solve_step_mt)(n, ld, r, m, tol, max_sweeps, depth, tx,
+                                    ty, ox, oy, u, work, b, rmax_out,
+                                    bmax_out, 1);
+}
+
 /*
  * Ten (or `steps`) backward-Euler steps from u = u⁰ (section 01: a run is
  * ten successive time steps): b = u + g, then solve to the stopping
@@ -337,19 +469,28 @@ long long FN(oracle_solve_step)(int n, long long ld, REAL r, int m,
  * sweeps[s] receives each step's count (or its negative status, after which
  * the run stops). Returns 0, or the first negative status.
  */
-long long FN(oracle_run)(int n, long long ld, REAL r, int m, double tol,
-                         long long max_sweeps, int depth, int tx, int ty,
-                         int ox, int oy, int steps, REAL *u, const REAL *g,
-                         REAL *work, REAL *b, long long *sweeps) {
+long long FN(oracle_run_mt)(int n, long long ld, REAL r, int m, double tol,
+                            long long max_sweeps, int depth, int tx, int ty,
+                            int ox, int oy, int steps, REAL *u, const REAL *g,
+                            REAL *work, REAL *b, long long *sweeps,
+                            int threads) {
     for (int s = 0; s < steps; ++s) {
         FN(oracle_rhs)(n, ld, u, g, b);
-        long long k = FN(oracle_solve_step)(n, ld, r, m, tol, max_sweeps,
-                                            depth, tx, ty, ox, oy, u, work, b,
-                                            0, 0);
+        long long k = FN(oracle_solve_step_mt)(n, ld, r, m, tol, max_sweeps,
+                                               depth, tx, ty, ox, oy, u, work,
+                                               b, 0, 0, threads);
         sweeps[s] = k;
         if (k < 0) return k;
     }
     return 0;
+}
+
+long long FN(oracle_run)(int n, long long ld, REAL r, int m, double tol,
+                         long long max_sweeps, int depth, int tx, int ty,
+                         int ox, int oy, int steps, REAL *u, const REAL *g,
+                         REAL *work, REAL *b, long long *sweeps) {
+    return FN(oracle_run_mt)(n, ld, r, m, tol, max_sweeps, depth, tx, ty, ox,
+                             oy, steps, u, g, work, b, sweeps, 1);
 }
 
 #undef FN
