@@ -89,7 +89,8 @@ typedef enum {
     /* Use a fixed-divisor division (one multiply and two fused multiply-adds
      * with the precomputed RN(1/d)) if an exhaustive check against IEEE
      * division over all finite float32 numerators passes for this d (run
-     * once per distinct d, about a millisecond); otherwise IEEE division. */
+     * once per distinct d and cached for the process, about 7 ms on
+     * GB300); otherwise IEEE division. */
     JACOBI_DIVISION_AUTO = 0,
     /* Always the IEEE division instruction sequence. */
     JACOBI_DIVISION_IEEE = 1
@@ -251,7 +252,11 @@ int jacobi_residual(jacobi_handle_t *h, float *rmax, float *bmax);
  * calls share it, so calls that could overlap on the GPU (other streams,
  * other host threads) race and must be serialised by the caller. The first
  * call on each device looks up the array's device address; make that first
- * call before any stream capture. It calls no allocating routine.
+ * call before any stream capture. Every later call enqueues one kernel and
+ * nothing else: the kernel's last block leaves the array ready for the next
+ * call. Only the first call after a call on the same device that returned
+ * JACOBI_ERR_CUDA also enqueues a 4-byte memset of the array's counter. It
+ * calls no allocating routine.
  *
  * Returns JACOBI_OK, JACOBI_ERR_INVALID_ARG (sizes, pitch, r, NULL or
  * misaligned pointers), JACOBI_ERR_UNSUPPORTED when N exceeds

@@ -28,7 +28,10 @@ constexpr int kRows = 32;
 constexpr unsigned FULL = 0xffffffffu;
 
 // Per-block partial maxima (2 words per block) followed by the last-block
-// ticket. Zero at load; the ticket is cleared again before every launch.
+// ticket. Zero at load. The last block of every launch sets the ticket back
+// to zero, so it is zero again whenever a launch has run to its end; it is
+// cleared explicitly only on the first call after a call on the same device
+// that failed (a launch that could not be enqueued or completed).
 constexpr int kMaxBlocks = JACOBI_RESIDUAL_NOALLOC_MAX_BLOCKS;
 constexpr int kTicket = 2 * kMaxBlocks;
 static __device__ __align__(256) unsigned g_residual_scratch[2 * kMaxBlocks + 64];
@@ -38,6 +41,8 @@ static __device__ __align__(256) unsigned g_residual_scratch[2 * kMaxBlocks + 64
 // stand-in, not a device address).
 constexpr int kMaxDevices = 64;
 unsigned *g_scratch_ptr[kMaxDevices] = {nullptr};
+// Per device: an earlier call failed, so the ticket may not be zero.
+bool g_ticket_suspect[kMaxDevices] = {false};
 std::mutex g_scratch_mutex;
 
 __device__ __forceinline__ float4 ld4(const float *p) {
@@ -172,7 +177,9 @@ k_residual_noalloc(const float *__restrict__ u, const float *__restrict__ b,
 }
 
 // Look up (once per device) the device address of the scratch array.
-cudaError_t scratch_for_current_device(unsigned **out) {
+// *suspect: whether an earlier call on this device failed (cleared here).
+cudaError_t scratch_for_current_device(unsigned **out, int *dev_out,
+                                       bool *suspect) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -185,7 +192,15 @@ cudaError_t scratch_for_current_device(unsigned **out) {
         g_scratch_ptr[dev] = static_cast<unsigned *>(p);
     }
     *out = g_scratch_ptr[dev];
+    *dev_out = dev;
+    *suspect = g_ticket_suspect[dev];
+    g_ticket_suspect[dev] = false;
     return cudaSuccess;
+}
+
+void mark_ticket_suspect(int dev) {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    g_ticket_suspect[dev] = true;
 }
 
 bool aligned16(const void *p) {
@@ -209,17 +224,27 @@ extern "C" int jacobi_residual_noalloc(int n, long long ld, float r,
     const long long gy = (n - 2 + kWarps * kRows - 1) / (kWarps * kRows);
     if (gx * gy > kMaxBlocks) return JACOBI_ERR_UNSUPPORTED;  // n too large
     unsigned *scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != cudaSuccess)
+    int dev = 0;
+    bool suspect = false;
+    if (scratch_for_current_device(&scratch, &dev, &suspect) != cudaSuccess)
         return JACOBI_ERR_CUDA;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    // The ticket must start at zero (a failed earlier launch could have left
-    // it set); the per-block partials are always written before use.
-    if (cudaMemsetAsync(scratch + kTicket, 0, sizeof(unsigned), stream) !=
-        cudaSuccess)
+    // The ticket is zero after every launch that ran to its end; after a
+    // failed call it is cleared once more. The per-block partials are always
+    // written before they are read.
+    if (suspect &&
+        cudaMemsetAsync(scratch + kTicket, 0, sizeof(unsigned), stream) !=
+            cudaSuccess) {
+        mark_ticket_suspect(dev);
         return JACOBI_ERR_CUDA;
+    }
     volatile float four_r = 4.0f * r;
     const float d = 1.0f + four_r;
     k_residual_noalloc<<<dim3((unsigned)gx, (unsigned)gy), dim3(32, kWarps), 0,
                          stream>>>(u, b, n, ld, r, d, scratch, norms);
-    return cudaGetLastError() == cudaSuccess ? JACOBI_OK : JACOBI_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) {
+        mark_ticket_suspect(dev);
+        return JACOBI_ERR_CUDA;
+    }
+    return JACOBI_OK;
 }

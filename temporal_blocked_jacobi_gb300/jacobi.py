@@ -123,9 +123,14 @@ def status_string(status: int) -> str:
 def residual_noalloc(u, b, r, norms, stream=None) -> int:
     """jacobi_residual_noalloc: residual norms of any (u, b) pair into the
     device tensor `norms` (2 floats: rmax, bmax) without allocating anything;
-    asynchronous on `stream` (default: the current torch stream). Returns the
-    status code (0 on success) instead of raising, so it can be used where
-    exceptions are unwelcome."""
+    asynchronous on `stream` (default: the current torch stream of u's
+    device). The call is made with u's device current, so u, b, norms and the
+    stream must all be on that device.
+
+    Raises ValueError when the tensors are not usable (wrong dtype, shape,
+    layout or device); otherwise returns the library's status code (0 on
+    success) instead of raising, so a caller inside stream capture can test
+    it without unwinding."""
     import torch
     _check_field(u)
     _check_field(b, u.shape)
@@ -133,10 +138,15 @@ def residual_noalloc(u, b, r, norms, stream=None) -> int:
             and norms.dtype == torch.float32 and norms.numel() >= 2
             and norms.is_contiguous()):
         raise ValueError("norms must be a contiguous float32 CUDA tensor of 2 elements")
+    if b.device != u.device or norms.device != u.device:
+        raise ValueError("u, b and norms must be on the same device")
     stream = torch.cuda.current_stream(u.device) if stream is None else stream
-    return int(load().jacobi_residual_noalloc(
-        int(u.shape[0]), int(u.shape[1]), float(r), _ptr(u), _ptr(b),
-        _ptr(norms), ctypes.c_void_p(stream.cuda_stream)))
+    if stream.device != u.device:
+        raise ValueError("the stream must belong to u's device")
+    with torch.cuda.device(u.device):
+        return int(load().jacobi_residual_noalloc(
+            int(u.shape[0]), int(u.shape[1]), float(r), _ptr(u), _ptr(b),
+            _ptr(norms), ctypes.c_void_p(stream.cuda_stream)))
 
 
 def adapt_depths(policy, depth_max, rhos, mss):
