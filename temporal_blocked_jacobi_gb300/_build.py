@@ -18,10 +18,13 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtbjacobi.so")
-SOURCES = ["kernels_sync.cu", "kernels_tiled.cu", "kernels_etb.cu",
-           "kernels_ba.cu", "kernels_bar.cu", "fastdiv.cu", "jacobi_abi.cu", "residual_noalloc.cu",
-           "adapt.cu"]
+# The four kernels_etb_part*.cu units come first: they take longest.
+SOURCES = ["kernels_etb_part0.cu", "kernels_etb_part1.cu", "kernels_etb_part2.cu",
+           "kernels_etb_part3.cu", "kernels_etb.cu", "kernels_sync.cu",
+           "kernels_tiled.cu", "kernels_ba.cu", "kernels_bar.cu", "fastdiv.cu",
+           "jacobi_abi.cu", "residual_noalloc.cu", "adapt.cu"]
 HEADERS = [os.path.join(CSRC, "jacobi_kernels.cuh"),
+           os.path.join(CSRC, "etb_kernels.cuh"),
            os.path.join(ROOT, "include", "jacobi.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -70,7 +73,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(res.stdout + res.stderr, flush=True)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]

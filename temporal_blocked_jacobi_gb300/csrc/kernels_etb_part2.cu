@@ -1,0 +1,8 @@
+// Exact-temporal-blocking kernels of the shapes whose PART is 2 in
+// TBJ_ETB_VARIANTS (etb_kernels.cuh); compiled on its own so that the four
+// parts build in parallel.
+#include "etb_kernels.cuh"
+
+namespace tbj {
+TBJ_ETB_DEFINE_PART(2)
+}  // namespace tbj
