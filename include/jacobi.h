@@ -338,6 +338,38 @@ int jacobi_adapt_next(jacobi_adapt_state_t *st, double rho, double ms);
  * 0 = IEEE division, < 0 = error (NULL handle). */
 int jacobi_division_mode(const jacobi_handle_t *h);
 
+/*
+ * Bounds-checked build. The pages have no counterpart for these calls; they
+ * serve testing. The same sources built with JACOBI_BOUNDS_CHECK give
+ * libtbjacobi_checked.so, with the same entry points and results, in which
+ * the tiled kernels (exact temporal blocking and block-async, all tile
+ * shapes) check every shared-memory access, plain global load, global store
+ * and TMA box load against its range. An access out of range is not
+ * performed; the launch's error word records it and the next call that
+ * reads that word (solve, residual) returns JACOBI_ERR_CUDA with the message
+ * "bounds check: ...". Nothing traps. Stores are allowed on interior cells
+ * only (rows and columns 1 .. N-2), never on the Dirichlet ring or the row
+ * padding. The checked build also fills each block's dynamic shared memory
+ * with NaN at kernel entry, and the destination field's interior with NaN
+ * before every sweep launch (not under JACOBI_CONTROL_PERSISTENT), so a
+ * value read before it was written, or an interior cell that a launch does
+ * not write, turns the result into NaN. It is slower and not meant for
+ * timing.
+ *
+ * jacobi_bounds_checked: 1 in the checked library, 0 otherwise.
+ * jacobi_bounds_selftest: runs the checker on five accesses of its own on
+ * the handle's u (one thread; synchronises the stream; allocates and frees
+ * 20 bytes of device memory): a shared-memory load past the region declared
+ * to the checker (bit 0), stores to a ring row (bit 1) and a ring column
+ * (bit 2) of u, a shared load inside the region (bit 3) and a store to
+ * interior cell (1, 1) (bit 4). Every store writes back the value the cell
+ * holds. Returns the mask of the accesses that were refused -- 0x7 when the
+ * checker works -- or a negative status; JACOBI_ERR_UNSUPPORTED in the
+ * unchecked library.
+ */
+int jacobi_bounds_checked(void);
+int jacobi_bounds_selftest(jacobi_handle_t *h);
+
 /* Number of kernels this handle has launched so far (graph nodes included). */
 long long jacobi_launch_count(const jacobi_handle_t *h);
 

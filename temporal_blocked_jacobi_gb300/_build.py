@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtbjacobi.so")
+# The bounds-checked variant (JACOBI_BOUNDS_CHECK; see include/jacobi.h):
+# same sources, its own objects.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libtbjacobi_checked.so")
 # The four kernels_etb_part*.cu units come first: they take longest.
 SOURCES = ["kernels_etb_part0.cu", "kernels_etb_part1.cu", "kernels_etb_part2.cu",
            "kernels_etb_part3.cu", "kernels_etb.cu", "kernels_sync.cu",
@@ -46,24 +50,27 @@ def nvcc() -> str:
     return path
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [__file__]
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libtbjacobi.so if any source changed. Returns its path."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link libtbjacobi.so (checked: libtbjacobi_checked.so) if
+    any source changed. Returns its path."""
+    lib, build_dir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
+    flags = NVCC_FLAGS + (["-DJACOBI_BOUNDS_CHECK"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -76,14 +83,21 @@ def build(force: bool = False, verbose: bool = False) -> str:
     workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False, verbose: bool = False):
+    """Both libraries, compiled side by side. Returns their paths."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        futs = [ex.submit(build, force, verbose, c) for c in (False, True)]
+        return [f.result() for f in futs]
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose=True))
+    print(build_all(force=True, verbose=True))

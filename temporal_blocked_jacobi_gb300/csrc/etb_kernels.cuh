@@ -118,12 +118,6 @@ struct EtbShape {
     static_assert(BX <= 256 && BY <= 256, "TMA box dimension limit");
 };
 
-__device__ __forceinline__ float4 lds4(const float *p) {
-    return *reinterpret_cast<const float4 *>(p);
-}
-__device__ __forceinline__ void sts4(float *p, float4 v) {
-    *reinterpret_cast<float4 *>(p) = v;
-}
 
 // One sweep of one tile. RESID: also reduce |J(u) - u| (first sweep of a
 // fused launch); LAST: write the tile to global memory instead of to dst.
@@ -191,12 +185,12 @@ __device__ __forceinline__ void etb_sweep(const float *src, float *dst, int s,
                 if (in_tile[c] && tile_row && row_ok) {
                     float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
                     if (colmask[c] == 0xfu) {
-                        sts4(g, nv);
+                        gst4(g, nv);
                     } else {
-                        if (colmask[c] & 1u) g[0] = nv.x;
-                        if (colmask[c] & 2u) g[1] = nv.y;
-                        if (colmask[c] & 4u) g[2] = nv.z;
-                        if (colmask[c] & 8u) g[3] = nv.w;
+                        if (colmask[c] & 1u) gst1(g + 0, nv.x);
+                        if (colmask[c] & 2u) gst1(g + 1, nv.y);
+                        if (colmask[c] & 4u) gst1(g + 2, nv.z);
+                        if (colmask[c] & 8u) gst1(g + 3, nv.w);
                     }
                 }
             }
@@ -263,8 +257,12 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *map_src,
             smem_addr(bar)),
         "r"((unsigned)(2 * S::BOX_BYTES))
         : "memory");
-    tma_load_2d(a, map_src, bar, gx0 - S::HX, gy0 - depth);
-    tma_load_2d(bb, map_b, bar, gx0 - S::HX, gy0 - depth);
+    // (checked build: a load that fails its check is not issued, and the
+    // wait for it runs into its time limit)
+    if (tma_ok(a, (unsigned)S::BOX_BYTES, gx0 - S::HX))
+        tma_load_2d(a, map_src, bar, gx0 - S::HX, gy0 - depth);
+    if (tma_ok(bb, (unsigned)S::BOX_BYTES, gx0 - S::HX))
+        tma_load_2d(bb, map_b, bar, gx0 - S::HX, gy0 - depth);
 }
 
 // Persistent kernel: block k handles tiles k, k + gridDim.x, ... (row-major
@@ -288,6 +286,7 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
     // each buffer = spare row, BY box rows, spare row; rows are 512 or 1024
     // bytes, so every box row is 128-byte aligned.
     extern __shared__ __align__(128) unsigned char smem_raw[];
+    bounds_begin(smem_raw, 0, out, nullptr, nullptr, nullptr, n, ld, err);
     const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + pad);
     float *buf0 = reinterpret_cast<float *>(smem_raw + pad + 128);
@@ -296,8 +295,8 @@ k_etb(const __grid_constant__ CUtensorMap map_src,
     const int tid = threadIdx.x;
     for (int k = tid; k < S::BX; k += 32 * NW)
         for (int q = 0; q < 2 * NB; ++q) {
-            buf0[q * bufn + k] = 0.f;  // spare rows: finite values
-            buf0[q * bufn + (S::BY + 1) * S::BX + k] = 0.f;
+            sts1(buf0 + q * bufn + k, 0.f);  // spare rows: finite values
+            sts1(buf0 + q * bufn + (S::BY + 1) * S::BX + k, 0.f);
         }
     if (tid == 0) {
         mbar_init(&bars[0]);
@@ -462,12 +461,12 @@ __device__ __forceinline__ void etbr_row(int j, float4 (&u)[RW][CH],
             if (in_tile[c] && tile_row && row_ok) {
                 float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
                 if (colmask[c] == 0xfu) {
-                    sts4(g, nv);
+                    gst4(g, nv);
                 } else {
-                    if (colmask[c] & 1u) g[0] = nv.x;
-                    if (colmask[c] & 2u) g[1] = nv.y;
-                    if (colmask[c] & 4u) g[2] = nv.z;
-                    if (colmask[c] & 8u) g[3] = nv.w;
+                    if (colmask[c] & 1u) gst1(g + 0, nv.x);
+                    if (colmask[c] & 2u) gst1(g + 1, nv.y);
+                    if (colmask[c] & 4u) gst1(g + 2, nv.z);
+                    if (colmask[c] & 8u) gst1(g + 3, nv.w);
                 }
             }
         }
@@ -615,6 +614,7 @@ k_etbr(const __grid_constant__ CUtensorMap map_src,
 
     // [barrier | u box | b box | exchange rows], box rows 512 or 1024 bytes.
     extern __shared__ __align__(128) unsigned char smem_raw[];
+    bounds_begin(smem_raw, 0, out, nullptr, nullptr, nullptr, n, ld, err);
     const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + pad);
     float *su = reinterpret_cast<float *>(smem_raw + pad + 128);
@@ -624,8 +624,8 @@ k_etbr(const __grid_constant__ CUtensorMap map_src,
     const int tid = threadIdx.x;
     for (int k = tid; k < S::BX; k += 32 * NW)
         for (int q = 0; q < 2; ++q) {
-            xb[q * S::XROWS * S::BX + k] = 0.f;  // slot -1
-            xb[(q * S::XROWS + S::XROWS - 1) * S::BX + k] = 0.f;  // slot 2 NW
+            sts1(xb + q * S::XROWS * S::BX + k, 0.f);  // slot -1
+            sts1(xb + (q * S::XROWS + S::XROWS - 1) * S::BX + k, 0.f);  // slot 2 NW
         }
     if (tid == 0) {
         mbar_init(bar);
@@ -781,6 +781,7 @@ k_etbp(const __grid_constant__ CUtensorMap map_u,
     __shared__ unsigned s_flag;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
+    bounds_begin(smem_raw, 0, u, u_alt, nullptr, nullptr, n, ld, &lp.state->err);
     const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + pad);
     float *su = reinterpret_cast<float *>(smem_raw + pad + 128);
@@ -791,8 +792,8 @@ k_etbp(const __grid_constant__ CUtensorMap map_u,
     LoopState *st = lp.state;
     for (int k = tid; k < S::BX; k += 32 * NW)
         for (int q = 0; q < 2; ++q) {
-            xb[q * S::XROWS * S::BX + k] = 0.f;
-            xb[(q * S::XROWS + S::XROWS - 1) * S::BX + k] = 0.f;
+            sts1(xb + q * S::XROWS * S::BX + k, 0.f);
+            sts1(xb + (q * S::XROWS + S::XROWS - 1) * S::BX + k, 0.f);
         }
     if (tid == 0) {
         mbar_init(bar);

@@ -249,6 +249,11 @@ cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
     const float *src = src_is_alt ? h->u_alt : h->u;
     float *dst = src_is_alt ? h->u : h->u_alt;
     const CUtensorMap *map_src = src_is_alt ? &h->map_alt : &h->map_u;
+    if (kBoundsChecked) {
+        // The launch must write every interior cell of dst.
+        cudaError_t e = launch_poison_interior(h->g, dst, ctl.stop, s);
+        if (e != cudaSuccess) return e;
+    }
     switch (h->cfg.strategy) {
         case JACOBI_SYNC:
             return launch_sweep_sync(h->g, src, h->b, dst, ctl, s);
@@ -776,12 +781,24 @@ int settle(jacobi_handle_t *h) {
     return JACOBI_OK;
 }
 
+// What the error bits a kernel left in its status word mean.
+const char *device_error_text(unsigned err) {
+    if (err & ERR_BOUNDS)
+        return "bounds check: a kernel access fell outside its buffer (checked "
+               "build; the access was not performed)";
+    if (err & ERR_TMA_TIMEOUT)
+        return "a TMA load did not complete within its wait limit";
+    if (err & ERR_SYNC_TIMEOUT)
+        return "a grid barrier of the persistent step did not complete within "
+               "its wait limit";
+    return "a kernel reported an error";
+}
+
 int check_device_status(jacobi_handle_t *h, unsigned err) {
-    if (err & ERR_TMA_TIMEOUT) {
+    if (err) {
         // Clear the word so the handle stays usable, then report.
         cudaMemsetAsync(&h->dev_out->err, 0, sizeof(unsigned), h->stream);
-        return fail(h, JACOBI_ERR_CUDA,
-                    "a TMA load did not complete within its wait limit");
+        return fail(h, JACOBI_ERR_CUDA, "%s", device_error_text(err));
     }
     return JACOBI_OK;
 }
@@ -922,13 +939,7 @@ static long long device_step_launches(const jacobi_handle_t *h,
 static long long device_step_outcome(jacobi_handle_t *h, const LoopState &st) {
     if (!st.stop)
         return fail(h, JACOBI_ERR_CUDA, "device loop ended without a decision");
-    if (st.err & ERR_TMA_TIMEOUT)
-        return fail(h, JACOBI_ERR_CUDA,
-                    "a TMA load did not complete within its wait limit");
-    if (st.err & ERR_SYNC_TIMEOUT)
-        return fail(h, JACOBI_ERR_CUDA,
-                    "a grid barrier of the persistent step did not complete "
-                    "within its wait limit");
+    if (st.err) return fail(h, JACOBI_ERR_CUDA, "%s", device_error_text(st.err));
     switch (st.status) {
         case 0:
             return st.result_k;
@@ -1207,6 +1218,34 @@ void jacobi_destroy(jacobi_handle_t *h) {
     if (h->loop_host) cudaFreeHost(h->loop_host);
     if (h->g_copy) cudaFree(h->g_copy);
     delete h;
+}
+
+int jacobi_bounds_checked(void) { return kBoundsChecked ? 1 : 0; }
+
+int jacobi_bounds_selftest(jacobi_handle_t *h) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (!kBoundsChecked)
+        return fail(h, JACOBI_ERR_UNSUPPORTED,
+                    "the bounds self-test needs the bounds-checked library");
+    constexpr int kChecks = 5;
+    unsigned *flags = nullptr;
+    TBJ_CUDA(h, cudaMalloc(&flags, kChecks * sizeof(unsigned)));
+    unsigned host[kChecks] = {0};
+    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof host, h->stream);
+    if (e == cudaSuccess)
+        e = launch_bounds_selftest(h->u, h->g.n, h->g.ld, flags, h->stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(host, flags, sizeof host, cudaMemcpyDeviceToHost,
+                            h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    cudaFree(flags);
+    if (e != cudaSuccess)
+        return fail(h, JACOBI_ERR_CUDA, "bounds self-test: %s",
+                    cudaGetErrorString(e));
+    int mask = 0;
+    for (int k = 0; k < kChecks; ++k)
+        if (host[k] & ERR_BOUNDS) mask |= 1 << k;
+    return mask;
 }
 
 const char *jacobi_last_error(const jacobi_handle_t *h) {

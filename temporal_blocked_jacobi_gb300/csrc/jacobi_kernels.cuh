@@ -136,7 +136,174 @@ float reciprocal_rn(float d);
 enum : unsigned {
     ERR_TMA_TIMEOUT = 1u,   // an mbarrier wait for a TMA load gave up
     ERR_SYNC_TIMEOUT = 2u,  // a grid-wide barrier wait gave up
+    ERR_BOUNDS = 4u,        // bounds-checked build: an access was out of range
 };
+
+// ---------------------------------------------------------------------------
+// Bounds-checked build.
+//
+// Compiled with JACOBI_BOUNDS_CHECK (libtbjacobi_checked.so, a testing aid
+// standing in for a memory checker), the tiled kernels -- k_etbr, k_etb,
+// k_bar, k_ba, k_block_async -- route every shared-memory access, every
+// plain global load of a grid and every global store through the accessors
+// below, and check every TMA box load's x coordinate and destination. An
+// access outside its range is not performed: it sets ERR_BOUNDS in the
+// launch's error word (reported as JACOBI_ERR_CUDA) and a load yields NaN.
+// Nothing traps. The ranges are
+//   * shared memory: the block's dynamic shared memory, [base, base + bytes),
+//     with the access aligned to its size;
+//   * plain global loads: the N x ld floats of a grid array;
+//   * global stores: interior cells of the output grid only (rows and
+//     columns 1 .. N-2) -- a store to the Dirichlet ring or the row padding
+//     is as wrong as one past the array;
+//   * TMA loads: x a multiple of 4 floats (the 16-byte rule), the box inside
+//     shared memory.
+// The checked build also poisons: bounds_begin() fills the block's dynamic
+// shared memory with NaN before anything else, and the host fills the
+// destination grid's interior with NaN before every sweep launch, so a cell
+// read before it was written, or an interior cell no launch writes, shows up
+// as NaN in the result.
+//
+// Without JACOBI_BOUNDS_CHECK the accessors are plain loads and stores.
+// ---------------------------------------------------------------------------
+#if defined(JACOBI_BOUNDS_CHECK)
+constexpr bool kBoundsChecked = true;
+#else
+constexpr bool kBoundsChecked = false;
+#endif
+
+// The range rules, as pure functions (also compiled and tested on the host).
+// off, bytes: byte offset and size of a shared access; limit: the region's
+// size in bytes.
+__host__ __device__ constexpr bool smem_access_ok(long long off, unsigned bytes,
+                                                  unsigned long long limit) {
+    return off >= 0 && bytes > 0 && (off % bytes) == 0 &&
+           (unsigned long long)off + bytes <= limit;
+}
+// idx, count: first float and number of floats of a global access to an
+// n x ld grid.
+__host__ __device__ constexpr bool grid_access_ok(long long idx, int count,
+                                                  int n, long long ld) {
+    return idx >= 0 && count > 0 && idx + count <= (long long)n * ld;
+}
+// The same access lies on interior cells only (one row, columns 1 .. n-2).
+__host__ __device__ constexpr bool interior_access_ok(long long idx, int count,
+                                                      int n, long long ld) {
+    return grid_access_ok(idx, count, n, ld) && idx / ld >= 1 &&
+           idx / ld <= n - 2 && idx % ld >= 1 && idx % ld + count - 1 <= n - 2;
+}
+// x coordinate of a TMA load of 4-byte elements.
+__host__ __device__ constexpr bool tma_x_ok(int x) { return (x & 3) == 0; }
+
+#if defined(JACOBI_BOUNDS_CHECK)
+namespace {
+struct BoundsCtx {
+    const unsigned char *smem;  // the block's dynamic shared memory
+    unsigned smem_bytes;
+    const float *out, *out2;    // output grids (stores); out2 may be null
+    const float *in0, *in1;     // grids read with plain loads, or null
+    long long ld;
+    int n;
+    unsigned *err;
+};
+__shared__ BoundsCtx g_bounds;
+}  // namespace
+
+__device__ __forceinline__ bool bounds_fail() {
+    atomicOr(g_bounds.err, (unsigned)ERR_BOUNDS);
+    return false;
+}
+__device__ __forceinline__ bool smem_ok(const void *p, unsigned bytes) {
+    const long long off = reinterpret_cast<const unsigned char *>(p) - g_bounds.smem;
+    return smem_access_ok(off, bytes, g_bounds.smem_bytes) || bounds_fail();
+}
+__device__ __forceinline__ bool store_ok(const float *p, int count) {
+    return interior_access_ok(p - g_bounds.out, count, g_bounds.n, g_bounds.ld) ||
+           (g_bounds.out2 &&
+            interior_access_ok(p - g_bounds.out2, count, g_bounds.n, g_bounds.ld)) ||
+           bounds_fail();
+}
+__device__ __forceinline__ bool load_ok(const float *base, const float *p, int count) {
+    const bool known = base == g_bounds.in0 || base == g_bounds.in1;
+    return (known && grid_access_ok(p - base, count, g_bounds.n, g_bounds.ld)) ||
+           bounds_fail();
+}
+__device__ __forceinline__ bool tma_ok(const void *dst, unsigned bytes, int x) {
+    return (tma_x_ok(x) && smem_access_ok(reinterpret_cast<const unsigned char *>(dst) -
+                                              g_bounds.smem,
+                                          16, g_bounds.smem_bytes) &&
+            smem_access_ok(reinterpret_cast<const unsigned char *>(dst) -
+                               g_bounds.smem + bytes - 16,
+                           16, g_bounds.smem_bytes)) ||
+           bounds_fail();
+}
+#else
+__device__ __forceinline__ bool smem_ok(const void *, unsigned) { return true; }
+__device__ __forceinline__ bool store_ok(const float *, int) { return true; }
+__device__ __forceinline__ bool load_ok(const float *, const float *, int) { return true; }
+__device__ __forceinline__ bool tma_ok(const void *, unsigned, int) { return true; }
+#endif
+
+// Start of a tiled kernel (every thread, before anything else). Checked
+// build: records what the block may touch -- `smem_bytes` bytes of dynamic
+// shared memory from `smem` (0: all of it), the output grids `out`, `out2`
+// (null: none), the grids `in0`, `in1` read with plain loads, n, ld, the
+// error word -- and fills the dynamic shared memory with NaN. Otherwise
+// nothing.
+__device__ __forceinline__ void bounds_begin(void *smem, unsigned smem_bytes,
+                                             const float *out, const float *out2,
+                                             const float *in0, const float *in1,
+                                             int n, long long ld, unsigned *err) {
+#if defined(JACOBI_BOUNDS_CHECK)
+    unsigned dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (smem_bytes == 0 || smem_bytes > dyn) smem_bytes = dyn;
+    const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+    const int nt = blockDim.x * blockDim.y * blockDim.z;
+    unsigned *w = reinterpret_cast<unsigned *>(smem);
+    for (unsigned k = tid; k < dyn / 4; k += nt) w[k] = 0x7fc0dead;  // NaN
+    if (tid == 0) {
+        g_bounds.smem = reinterpret_cast<const unsigned char *>(smem);
+        g_bounds.smem_bytes = smem_bytes;
+        g_bounds.out = out;
+        g_bounds.out2 = out2;
+        g_bounds.in0 = in0;
+        g_bounds.in1 = in1;
+        g_bounds.ld = ld;
+        g_bounds.n = n;
+        g_bounds.err = err;
+    }
+    __syncthreads();
+#else
+    (void)smem, (void)smem_bytes, (void)out, (void)out2, (void)in0, (void)in1,
+        (void)n, (void)ld, (void)err;
+#endif
+}
+
+// Shared-memory loads and stores of a float4 (16-byte aligned) or a float.
+__device__ __forceinline__ float4 lds4(const float *p) {
+    if (!smem_ok(p, 16)) {
+        const float q = __int_as_float(0x7fc00000);
+        return make_float4(q, q, q, q);
+    }
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ void sts4(float *p, float4 v) {
+    if (smem_ok(p, 16)) *reinterpret_cast<float4 *>(p) = v;
+}
+__device__ __forceinline__ float lds1(const float *p) {
+    return smem_ok(p, 4) ? *p : __int_as_float(0x7fc00000);
+}
+__device__ __forceinline__ void sts1(float *p, float v) {
+    if (smem_ok(p, 4)) *p = v;
+}
+// Global stores into the output grid's interior.
+__device__ __forceinline__ void gst4(float *p, float4 v) {
+    if (store_ok(p, 4)) *reinterpret_cast<float4 *>(p) = v;
+}
+__device__ __forceinline__ void gst1(float *p, float v) {
+    if (store_ok(p, 1)) *p = v;
+}
 
 // Parameters common to all sweep kernels.
 struct GridDesc {
@@ -333,6 +500,18 @@ cudaError_t launch_rhs(const GridDesc &g, const float *u, const float *src,
                        float *b, cudaStream_t stream);
 cudaError_t launch_copy_interior(const GridDesc &g, const float *src,
                                  float *dst, cudaStream_t stream);
+// Bounds-checked build only: NaN into dst's interior unless *stop is set
+// (stop may be null).
+cudaError_t launch_poison_interior(const GridDesc &g, float *dst,
+                                  const int *stop, cudaStream_t stream);
+// Bounds-checked build only: exercise the checker on `grid` (n x ld
+// floats): flags[k] receives ERR_BOUNDS if check k refused its access.
+// Checks 0-2 are out of range (a shared load past the region declared to
+// the checker, stores to a ring row and to a ring column of `grid`), 3-4
+// in range (a shared load inside it, a store to an interior cell). Every
+// store writes the value the cell already holds.
+cudaError_t launch_bounds_selftest(float *grid, int n, long long ld,
+                                   unsigned *flags, cudaStream_t stream);
 cudaError_t launch_sweep_sync(const GridDesc &g, const float *u,
                               const float *b, float *out,
                               const LaunchCtl &ctl, cudaStream_t stream);
@@ -432,7 +611,8 @@ bool ba_reg_configure(int n, TileConf *tc);
 cudaError_t prepare_sweep_ba_reg();
 cudaError_t launch_sweep_ba_reg(const GridDesc &g, const TileConf &tc,
                                 const float *src, const float *b, float *out,
-                                const LaunchCtl &ctl, cudaStream_t stream);
+                                unsigned *err, const LaunchCtl &ctl,
+                                cudaStream_t stream);
 // Streaming block-asynchronous kernel (kernels_ba.cu).
 bool ba_stream_configure(int n, TileConf *tc);
 cudaError_t prepare_sweep_ba_stream(const TileConf &tc);

@@ -74,12 +74,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
         : "memory");
 }
 
-__device__ __forceinline__ float4 lds4(const float *p) {
-    return *reinterpret_cast<const float4 *>(p);
-}
-__device__ __forceinline__ void sts4(float *p, float4 v) {
-    *reinterpret_cast<float4 *>(p) = v;
-}
 
 // J for the four cells of a chunk. ex = east neighbour of .x, wy = west
 // neighbour of .y (the chunk's own .y/.x unless a BA tile edge lies between).
@@ -213,12 +207,12 @@ __device__ __forceinline__ void ba_sweeps(const float *sA, float *sB, float *sC,
                     } else if (row_ok && keep[c]) {
                         float *g = out + (long long)gy * ld + (bxo + 128 * c + col);
                         if (keep[c] == 0xfu) {
-                            sts4(g, nv);
+                            gst4(g, nv);
                         } else {
-                            if (keep[c] & 1u) g[0] = nv.x;
-                            if (keep[c] & 2u) g[1] = nv.y;
-                            if (keep[c] & 4u) g[2] = nv.z;
-                            if (keep[c] & 8u) g[3] = nv.w;
+                            if (keep[c] & 1u) gst1(g + 0, nv.x);
+                            if (keep[c] & 2u) gst1(g + 1, nv.y);
+                            if (keep[c] & 4u) gst1(g + 2, nv.z);
+                            if (keep[c] & 8u) gst1(g + 3, nv.w);
                         }
                     }
                     nr[c] = cr[c];
@@ -244,6 +238,7 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
     const int byo = blockIdx.y * sy;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
+    bounds_begin(smem_raw, 0, out, nullptr, nullptr, nullptr, n, ld, err);
     const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + pad);
     float *sA = reinterpret_cast<float *>(smem_raw + pad + 128);
@@ -265,8 +260,11 @@ k_ba(const __grid_constant__ CUtensorMap map_src,
                 smem_addr(bar)),
             "r"((unsigned)(2 * BX * (sy + 2) * sizeof(float)))
             : "memory");
-        tma_load_2d(sA, &map_src, bar, bxo, byo);
-        tma_load_2d(sC, &map_b, bar, bxo, byo);  // b staged in C
+        const unsigned box = (unsigned)(BX * (sy + 2) * sizeof(float));
+        // (checked build: a load that fails its check is not issued, and
+        // the wait for it runs into its time limit)
+        if (tma_ok(sA, box, bxo)) tma_load_2d(sA, &map_src, bar, bxo, byo);
+        if (tma_ok(sC, box, bxo)) tma_load_2d(sC, &map_b, bar, bxo, byo);  // b staged in C
     }
     __syncthreads();
     const bool ok = mbar_wait_bounded(bar);

@@ -37,9 +37,6 @@ constexpr int kTX = 32, kTY = 8;  // the BA tile
 constexpr int kWarps = 4;         // strips per block
 constexpr int kMinBlocks = 3;     // blocks per SM the registers are sized for
 
-__device__ __forceinline__ float4 lds4(const float *p) {
-    return *reinterpret_cast<const float4 *>(p);
-}
 
 // Columns 4 l + 1 .. 4 l + 4 of an aligned row segment from the two chunks
 // that cover columns 4 l .. 4 l + 7.
@@ -47,17 +44,21 @@ __device__ __forceinline__ float4 shift1(float4 a, float4 b) {
     return make_float4(a.y, a.z, a.w, b.x);
 }
 
-// Asynchronous global -> shared copies of 16 or 4 bytes; src_bytes = 0
-// writes zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src,
+// Asynchronous global -> shared copies of 16 or 4 bytes from grid `base`;
+// src_bytes = 0 writes zeros and reads nothing. (Checked build: the copy is
+// dropped when its destination or source is out of range.)
+__device__ __forceinline__ void cp_async16(float *dst, const float *base,
+                                           const float *src,
                                            unsigned src_bytes) {
+    if (!smem_ok(dst, 16) || (src_bytes && !load_ok(base, src, 4))) return;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
                      static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                  "l"(src), "r"(src_bytes)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async4(void *dst, const void *src,
-                                          unsigned src_bytes) {
+__device__ __forceinline__ void cp_async4(float *dst, const float *base,
+                                          const float *src, unsigned src_bytes) {
+    if (!smem_ok(dst, 4) || (src_bytes && !load_ok(base, src, 1))) return;
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
                      static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                  "l"(src), "r"(src_bytes)
@@ -104,17 +105,17 @@ __device__ __forceinline__ void bar_strip(const float *__restrict__ src,
         const float *row = src + (long long)(row_in ? gy : 0) * ld;
         float *srow = su + (j + 1) * kURow;
         const bool a_in = row_in && c0 < ld;
-        cp_async16(srow + 4 * lane, a_in ? row + c0 : src, a_in ? 16u : 0u);
+        cp_async16(srow + 4 * lane, src, a_in ? row + c0 : src, a_in ? 16u : 0u);
         if (lane == 31) {
             const bool b_in = row_in && c0 + 4 < ld;
-            cp_async16(srow + 128, b_in ? row + c0 + 4 : src, b_in ? 16u : 0u);
+            cp_async16(srow + 128, src, b_in ? row + c0 + 4 : src, b_in ? 16u : 0u);
         }
         if (j >= 0 && j < kTY) {
             const float *brow = bsrc + (long long)(row_in ? gy : 0) * ld;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const bool in = row_in && gx0 + k < ld;
-                cp_async4(sbl + 128 * j + k, in ? brow + gx0 + k : bsrc,
+                cp_async4(sbl + 128 * j + k, bsrc, in ? brow + gx0 + k : bsrc,
                           in ? 4u : 0u);
             }
         }
@@ -182,15 +183,15 @@ __device__ __forceinline__ void bar_strip(const float *__restrict__ src,
         if (EDGE && gy > n - 2) break;
         float *o = out + (long long)gy * ld + gx0;
         if (!EDGE || colmask == 0xfu) {
-            o[0] = u[j].x;
-            o[1] = u[j].y;
-            o[2] = u[j].z;
-            o[3] = u[j].w;
+            gst1(o + 0, u[j].x);
+            gst1(o + 1, u[j].y);
+            gst1(o + 2, u[j].z);
+            gst1(o + 3, u[j].w);
         } else {
-            if (colmask & 1u) o[0] = u[j].x;
-            if (colmask & 2u) o[1] = u[j].y;
-            if (colmask & 4u) o[2] = u[j].z;
-            if (colmask & 8u) o[3] = u[j].w;
+            if (colmask & 1u) gst1(o + 0, u[j].x);
+            if (colmask & 2u) gst1(o + 1, u[j].y);
+            if (colmask & 4u) gst1(o + 2, u[j].z);
+            if (colmask & 8u) gst1(o + 3, u[j].w);
         }
     }
 }
@@ -199,9 +200,11 @@ template <bool FAST, bool FUSED>
 __global__ void __launch_bounds__(32 * kWarps, kMinBlocks)
 k_bar(const float *__restrict__ src, const float *__restrict__ bsrc,
       float *__restrict__ out, int n, long long ld, float r, float d, float y,
-      int depth, int units_x, int units, const int *stop, LoopParams lp) {
+      int depth, int units_x, int units, unsigned *err, const int *stop,
+      LoopParams lp) {
     __shared__ unsigned fin_scratch[33];
     extern __shared__ __align__(16) float smem[];  // kWarps slices
+    bounds_begin(smem, 0, out, nullptr, src, bsrc, n, ld, err);
     allow_dependents();
     // Everything below reads what the previous kernel wrote.
     grid_dependency_wait();
@@ -255,13 +258,14 @@ bool ba_reg_configure(int n, TileConf *tc) {
 
 cudaError_t launch_sweep_ba_reg(const GridDesc &g, const TileConf &tc,
                                 const float *src, const float *b, float *out,
-                                const LaunchCtl &ctl, cudaStream_t stream) {
+                                unsigned *err, const LaunchCtl &ctl,
+                                cudaStream_t stream) {
     const int units_x = (g.n - 2 + 127) / 128, units_y = (g.n - 2 + kTY - 1) / kTY;
     const int units = units_x * units_y;
 #define TBJ_K(F, FU)                                                         \
     launch_pdl(k_bar<F, FU>, dim3(tc.grid_x), dim3(32 * kWarps), kSmemBytes, \
                stream, src, b, out, g.n, g.ld, g.r, g.d, g.y, tc.depth,      \
-               units_x, units, ctl.stop, ctl.lp)
+               units_x, units, err, ctl.stop, ctl.lp)
     if (g.fast) return ctl.fused ? TBJ_K(true, true) : TBJ_K(true, false);
     return ctl.fused ? TBJ_K(false, true) : TBJ_K(false, false);
 #undef TBJ_K

@@ -318,6 +318,47 @@ __global__ void k_copy_interior(const float *__restrict__ src,
     }
 }
 
+// Bounds-checked build: NaN into every interior cell of dst ahead of a sweep
+// launch, which must write all of them. It honours the stop flag as the
+// sweep kernels do, so an answer that a device-side stop left in dst is
+// kept.
+__global__ void k_poison_interior(float *__restrict__ dst, int n, long long ld,
+                                  const int *stop) {
+    if (stop && *stop) return;
+    const float q = __int_as_float(0x7fc0bad0);
+    for (int i = 1 + blockIdx.y * blockDim.y + threadIdx.y; i <= n - 2;
+         i += gridDim.y * blockDim.y)
+        for (int j = 1 + blockIdx.x * blockDim.x + threadIdx.x; j <= n - 2;
+             j += gridDim.x * blockDim.x)
+            dst[(long long)i * ld + j] = q;
+}
+
+// Bounds-checked build: the checker's own test (launch_bounds_selftest).
+// One thread runs five accesses, each against its own error word; the
+// refused ones would be harmless even if performed: the shared load stays
+// inside the block's allocation (past the part declared to the checker),
+// and every store writes back the value the cell holds.
+__global__ void k_bounds_selftest(float *grid, int n, long long ld,
+                                  unsigned *flags) {
+    extern __shared__ __align__(16) float sm[];  // 256 bytes
+    bounds_begin(sm, 128, grid, nullptr, nullptr, nullptr, n, ld, flags);
+#if defined(JACOBI_BOUNDS_CHECK)
+    if (threadIdx.x != 0) return;
+    volatile float sink = 0.f;
+    g_bounds.err = flags + 0;
+    sink = lds1(sm + 40);  // byte 160 of a 128-byte region
+    g_bounds.err = flags + 1;
+    gst1(grid + 2, grid[2]);  // row 0: the ring
+    g_bounds.err = flags + 2;
+    gst1(grid + ld + (n - 1), grid[ld + (n - 1)]);  // column n-1: the ring
+    g_bounds.err = flags + 3;
+    sink = lds1(sm + 4);  // inside the region
+    g_bounds.err = flags + 4;
+    gst1(grid + ld + 1, grid[ld + 1]);  // interior cell (1, 1)
+    (void)sink;
+#endif
+}
+
 // Reset a step's loop state. In a graph of several time steps `prev` is the
 // previous step's state: if that step did not converge, this step is marked
 // skipped (stopped before it starts), so every later kernel of it returns at
@@ -381,6 +422,19 @@ cudaError_t launch_rhs(const GridDesc &g, const float *u, const float *src,
                        float *b, cudaStream_t stream) {
     k_rhs<<<elementwise_grid(g.n), dim3(32, 8), 0, stream>>>(u, src, b, g.n,
                                                               g.ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_poison_interior(const GridDesc &g, float *dst,
+                                  const int *stop, cudaStream_t stream) {
+    k_poison_interior<<<elementwise_grid(g.n), dim3(32, 8), 0, stream>>>(
+        dst, g.n, g.ld, stop);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bounds_selftest(float *grid, int n, long long ld,
+                                   unsigned *flags, cudaStream_t stream) {
+    k_bounds_selftest<<<1, 32, 256, stream>>>(grid, n, ld, flags);
     return cudaGetLastError();
 }
 

@@ -115,6 +115,8 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
               LoopParams lp) {
     if (stop && *stop) return;  // same value for every thread of the launch
     __shared__ unsigned fin_scratch[33];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    bounds_begin(smem_raw, 0, out, nullptr, nullptr, nullptr, n, ld, err);
     const int tx = tg.tx, ty = tg.ty, box_x = tg.box_x, box_y = tg.box_y;
     const int gx0 = 1 + blockIdx.x * tg.sx;  // tile's first cell (grid)
     const int gy0 = 1 + blockIdx.y * tg.sy;
@@ -134,7 +136,6 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
 
     // Offsets from the __shared__ array itself keep every access in the
     // shared address space.
-    extern __shared__ __align__(128) unsigned char smem_raw[];
     const unsigned pad = (128u - (smem_addr(smem_raw) & 127u)) & 127u;
     unsigned char *base = smem_raw + pad;
     uint64_t *bar = reinterpret_cast<uint64_t *>(base);
@@ -148,9 +149,11 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
         mbar_init(bar, 1);
         const unsigned box_bytes = (unsigned)(box_x * box_y * sizeof(float));
         mbar_arrive_expect_tx(bar, 3u * box_bytes);
-        tma_load_2d(sA, &map_src, bar, bxo, byo);
-        tma_load_2d(sB, &map_src, bar, bxo, byo);
-        tma_load_2d(sBb, &map_b, bar, bxo, byo);
+        // (checked build: a load that fails its check is not issued, and
+        // the wait for it runs into its time limit)
+        if (tma_ok(sA, box_bytes, bxo)) tma_load_2d(sA, &map_src, bar, bxo, byo);
+        if (tma_ok(sB, box_bytes, bxo)) tma_load_2d(sB, &map_src, bar, bxo, byo);
+        if (tma_ok(sBb, box_bytes, bxo)) tma_load_2d(sBb, &map_b, bar, bxo, byo);
     }
     __syncthreads();
     const bool ok = mbar_wait_bounded(bar);
@@ -183,17 +186,17 @@ k_block_async(const __grid_constant__ CUtensorMap map_src,
             const int gy = byo + by;
             const bool own_row = gy >= wy0 && gy < wy1;
             for (int bx = c0 + lane; bx < c1; bx += 32) {
-                const float w = row[bx - 1], e = row[bx + 1];
-                const float nn = row[bx - box_x], ss = row[bx + box_x];
-                const float v = jacobi_update<FAST>(w, e, nn, ss, brow[bx], r, d, y);
+                const float w = lds1(row + bx - 1), e = lds1(row + bx + 1);
+                const float nn = lds1(row + bx - box_x), ss = lds1(row + bx + box_x);
+                const float v = jacobi_update<FAST>(w, e, nn, ss, lds1(brow + bx), r, d, y);
                 const int gx = bxo + bx;
                 const bool own = own_row && gx >= wx0 && gx < wx1;
                 if (FUSED && s == 0 && own)  // |J(u) - u| of the launch's input
-                    rm = max(rm, change_bits(v, row[bx]));
+                    rm = max(rm, change_bits(v, lds1(row + bx)));
                 if (last) {
-                    if (own) out[(long long)gy * ld + gx] = v;
+                    if (own) gst1(out + (long long)gy * ld + gx, v);
                 } else {
-                    dst[by * box_x + bx] = v;
+                    sts1(dst + by * box_x + bx, v);
                 }
             }
         }
@@ -338,7 +341,7 @@ cudaError_t launch_sweep_ba(const GridDesc &g, const TileConf &tc,
                             const LaunchCtl &ctl, cudaStream_t stream) {
     unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
     if (tc.stream == 2)
-        return launch_sweep_ba_reg(g, tc, src, b, out, ctl, stream);
+        return launch_sweep_ba_reg(g, tc, src, b, out, err, ctl, stream);
     if (tc.stream)
         return launch_sweep_ba_stream(g, tc, map_src, map_b, out, err, ctl,
                                       stream);

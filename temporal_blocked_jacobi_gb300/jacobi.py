@@ -62,22 +62,22 @@ class JacobiError(RuntimeError):
         self.status = status
 
 
-_lib = None
+_libs = {}
 _lock = threading.Lock()
 
 
-def library_path() -> str:
-    return _build.LIB
+def library_path(checked: bool = False) -> str:
+    return _build.LIB_CHECKED if checked else _build.LIB
 
 
-def load():
-    """Load libtbjacobi.so (it must have been built by __graft_entry__.build()
-    or temporal_blocked_jacobi_gb300._build.build())."""
-    global _lib
+def load(checked: bool = False):
+    """Load libtbjacobi.so, or with checked=True its bounds-checked variant
+    libtbjacobi_checked.so (built by __graft_entry__.build() or
+    temporal_blocked_jacobi_gb300._build.build_all())."""
     with _lock:
-        if _lib is not None:
-            return _lib
-        path = library_path()
+        if checked in _libs:
+            return _libs[checked]
+        path = library_path(checked)
         if not os.path.exists(path):
             raise RuntimeError(
                 f"CUDA library {path} is missing; build it first "
@@ -104,12 +104,14 @@ def load():
             "jacobi_adapt_init": (i, [ctypes.POINTER(AdaptState), i, i]),
             "jacobi_adapt_next": (i, [ctypes.POINTER(AdaptState), ctypes.c_double,
                                       ctypes.c_double]),
+            "jacobi_bounds_checked": (i, []),
+            "jacobi_bounds_selftest": (i, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        _lib = lib
+        _libs[checked] = lib
         return lib
 
 
@@ -219,9 +221,10 @@ class Solver:
     def __init__(self, u, u_alt, b, r, *, strategy="sync", depth=1,
                  tile=(0, 0), check_every=8, tol=1e-5, max_sweeps=1 << 22,
                  control="host", division="auto", rhs="fused", adapt="none",
-                 overlap=(0, 0), stream=None):
+                 overlap=(0, 0), stream=None, checked=False):
         import torch
-        lib = load()
+        lib = load(checked)
+        self._lib = lib
         for t in (u, u_alt, b):
             _check_field(t, u.shape)
         self.n, self.ld = int(u.shape[0]), int(u.shape[1])
@@ -242,7 +245,7 @@ class Solver:
 
     # -- helpers -----------------------------------------------------------
     def _raise(self, status):
-        raise JacobiError(int(status), load().jacobi_last_error(self._h).decode())
+        raise JacobiError(int(status), self._lib.jacobi_last_error(self._h).decode())
 
     def _ok(self, rc):
         if rc < 0:
@@ -258,33 +261,39 @@ class Solver:
     # -- C ABI ---------------------------------------------------------------
     def rhs(self, g):
         _check_field(g, self.u.shape)
-        self._ok(load().jacobi_rhs(self.handle, _ptr(g)))
+        self._ok(self._lib.jacobi_rhs(self.handle, _ptr(g)))
 
     def solve_step(self, raise_on_error=True) -> int:
-        k = load().jacobi_solve_step(self.handle)
+        k = self._lib.jacobi_solve_step(self.handle)
         return self._ok(k) if raise_on_error else k
 
     def sweeps(self, launches: int) -> int:
-        return self._ok(load().jacobi_sweeps(self.handle, int(launches)))
+        return self._ok(self._lib.jacobi_sweeps(self.handle, int(launches)))
 
     def residual(self):
         rm, bm = ctypes.c_float(), ctypes.c_float()
-        self._ok(load().jacobi_residual(self.handle, ctypes.byref(rm), ctypes.byref(bm)))
+        self._ok(self._lib.jacobi_residual(self.handle, ctypes.byref(rm), ctypes.byref(bm)))
         return rm.value, bm.value
+
+    def bounds_selftest(self) -> int:
+        """jacobi_bounds_selftest (bounds-checked library only): the mask of
+        the checker's five test accesses that it refused (0x7 when it
+        works)."""
+        return self._ok(self._lib.jacobi_bounds_selftest(self.handle))
 
     def set_strategy(self, strategy="sync", depth=1, tile=(0, 0),
                      check_every=8, tol=1e-5, max_sweeps=1 << 22, control="host",
                      division="auto", rhs="fused", adapt="none", overlap=(0, 0)):
         cfg = make_config(strategy, depth, tile, check_every, tol, max_sweeps,
                           control, division, rhs, adapt, overlap)
-        self._ok(load().jacobi_set_strategy(self.handle, ctypes.byref(cfg)))
+        self._ok(self._lib.jacobi_set_strategy(self.handle, ctypes.byref(cfg)))
         self.config = cfg
 
     def run(self, g, steps=10):
         """`steps` backward-Euler steps; returns the list of sweeps per step."""
         _check_field(g, self.u.shape)
         counts = (ctypes.c_longlong * max(steps, 1))()
-        total = load().jacobi_run(self.handle, _ptr(g), int(steps), counts)
+        total = self._lib.jacobi_run(self.handle, _ptr(g), int(steps), counts)
         if total < 0:
             self._raise(total)
         return [int(counts[s]) for s in range(steps)]
@@ -292,7 +301,7 @@ class Solver:
     def check_trace(self):
         """The last solve_step's checks: list of dicts (depth, sweeps, rmax,
         bmax, ms); empty under device control."""
-        lib = load()
+        lib = self._lib
         n = lib.jacobi_check_trace(self.handle, None, 0)
         if n < 0:
             self._raise(n)
@@ -304,19 +313,19 @@ class Solver:
     @property
     def division_mode(self) -> int:
         """1 if the kernels use the verified fixed-divisor division, 0 if IEEE."""
-        return int(self._ok(load().jacobi_division_mode(self.handle)))
+        return int(self._ok(self._lib.jacobi_division_mode(self.handle)))
 
     @property
     def launch_count(self) -> int:
-        return int(load().jacobi_launch_count(self.handle))
+        return int(self._lib.jacobi_launch_count(self.handle))
 
     @property
     def last_error(self) -> str:
-        return load().jacobi_last_error(self.handle).decode()
+        return self._lib.jacobi_last_error(self.handle).decode()
 
     def close(self):
         if self._h:
-            load().jacobi_destroy(self._h)
+            self._lib.jacobi_destroy(self._h)
             self._h = ctypes.c_void_p()
 
     def __enter__(self):
