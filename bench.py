@@ -167,7 +167,10 @@ def roofline_record(kw, interior, launch_ms, working_set, l2_bytes, sms,
     alu = {"achieved": ops, "peak": alu_peak, "unit": "Top/s", "frac": ops / alu_peak,
            "peak_source": (f"{FP32_LANES_PER_SM} FP32 lanes x {sms} SMs x {mhz:.0f} MHz "
                            f"(maximum SM clock, {mhz_how})"),
-           "ops_per_lup": FP32_OPS_PER_LUP}
+           "ops_per_lup": FP32_OPS_PER_LUP,
+           # the same with the division counted as one operation (7 flops
+           # per lattice update: 3 adds, 1 multiply, 1 add, 1 division)
+           "frac_at_7_flops_per_lup": 7 * lups / 1e12 / alu_peak}
     l2_resident = working_set < l2_bytes
     bound = "alu" if l2_resident else "hbm"
     main = alu if bound == "alu" else hbm
@@ -618,12 +621,14 @@ def end_to_end(solver, u, g, u0_host, g_host, stream, interior, args):
 # CPU oracle legs (test infrastructure, timed as a reported baseline)
 # ---------------------------------------------------------------------------
 class OracleSample:
-    """The oracle (single-threaded C) timed on a bounded sample of the
-    ten-step solve: the first `sweeps` sweeps, right-hand sides and residual
-    checks included, continuing into later time steps as each one converges.
-    The inputs are built once, outside the timed calls."""
+    """The oracle (single-threaded C; `threads` > 1: its row-parallel form,
+    bit-identical) timed on a bounded sample of the ten-step solve: the first
+    `sweeps` sweeps, right-hand sides and residual checks included,
+    continuing into later time steps as each one converges. The inputs are
+    built once, outside the timed calls."""
 
-    def __init__(self, n, r, source):
+    def __init__(self, n, r, source, threads=1):
+        self.threads = threads
         import oracle
         self.oracle = oracle
         self.n, self.r = n, r
@@ -638,7 +643,8 @@ class OracleSample:
         t0 = time.perf_counter()
         while done < sample_sweeps and steps < TIME_STEPS:
             b = oracle.rhs(u, self.g)
-            k, _, _ = oracle.solve_step(u, b, self.r, max_sweeps=sample_sweeps - done)
+            k, _, _ = oracle.solve_step(u, b, self.r, max_sweeps=sample_sweeps - done,
+                                        threads=self.threads)
             done += (sample_sweeps - done) if k < 0 else k
             steps += 1
         dt = time.perf_counter() - t0
@@ -654,11 +660,19 @@ def cpu_baseline(args):
     n, r, source, _ = WORKLOADS[args.workload]
     # about 1e10 lattice updates: 10-15 s on one host core
     sweeps = args.cpu_sample_sweeps or max(8, int(8 * round(1.0e10 / (n - 2) ** 2 / 8)))
-    glups, dt, done = oracle_sample(n, r, source, sweeps)
+    sample = OracleSample(n, r, source)
+    glups, dt, done = sample(sweeps)
+    cores = os.cpu_count() or 1
+    sample.threads = cores
+    glups_all, dt_all, _ = sample(sweeps)
     return {"value": glups, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {done} sweeps of the ten-step solve (checks every 8), "
                       f"single-threaded C oracle, {dt:.1f} s",
-            "host_cpus": os.cpu_count()}
+            "host_cpus": cores,
+            # the same sample with the oracle's rows split over every host
+            # core (bit-identical results)
+            "all_cores": {"value": glups_all, "unit": UNIT, "cores": cores,
+                          "seconds": dt_all}}
 
 
 def run_reference(args):
