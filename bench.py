@@ -545,7 +545,8 @@ def kernel_roofline(solver, tok, u, u0, stream, interior, workload):
     # u, u_alt and b
     rec = roofline_record(kw, interior, ms, 3 * u.numel() * 4, props.L2_cache_size,
                           props.multi_processor_count, hbm_peak, hbm_how, mhz, mhz_how)
-    rec["kernel"] = kernel_name(tok)
+    rec["kernel"] = kernel_name(tok, solver.tile)
+    rec["tile"] = list(solver.tile)
     rec["launches_timed"] = launches
     rec["traffic"] = load_traffic(tok, workload)
     return rec
@@ -557,11 +558,15 @@ ETBR_TILES = {4: ((0, 0), (120, 88), (120, 40)), 8: ((0, 0), (112, 80), (112, 92
               16: ((0, 0), (96, 64), (96, 76))}
 
 
-def kernel_name(tok):
+def kernel_name(tok, tile=None):
+    """The sweep kernel of strategy `tok`; `tile`: the tile the solver
+    resolved (Solver.tile), which tells the column-streamed kernel apart."""
     kw = parse_strategy(tok)
     if kw["strategy"] == "sync":
         return "k_sweep_sync" + (" (unfused rhs)" if kw.get("rhs") == "unfused" else "")
     if kw["strategy"] == "etb":
+        if (tile or kw.get("tile", (0, 0)))[1] == 0 and (tile or kw.get("tile"))[0] > 0:
+            return f"k_etbs (D={kw['depth']}, column-streamed)"
         # default shapes: bands in registers for D = 4, 8 and 16, box in
         # shared memory for D = 2; explicit tiles of the band shapes likewise
         name = ("k_etbr" if kw.get("tile", (0, 0)) in ETBR_TILES.get(kw["depth"], ())

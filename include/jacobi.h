@@ -144,7 +144,13 @@ typedef struct {
                              register-resident shape that leaves each SM the
                              fewest box rows (D = 4: 120 x 88; D = 8: 112 x 80
                              or 112 x 92; D = 16: 96 x 64 or 96 x 76); D = 2:
-                             120 x 92. Any shape gives the same bits. */
+                             120 x 92. At D = 8, on grids with enough rows
+                             per warp (n from about 6000 on GB300; not under
+                             JACOBI_CONTROL_PERSISTENT), the default is
+                             112 x 0: tile_y = 0 selects the column-streamed
+                             kernel, in which each warp sweeps a 112-column
+                             strip D times as a pipeline down its rows (D = 8
+                             only). Any shape gives the same bits. */
     int check_every;      /* M: residual checked every lcm(M, sweeps per launch) sweeps; default 8 */
     double tol;           /* stop when rmax < tol * bmax (or rmax == 0); default 1e-5 */
     long long max_sweeps; /* give up (JACOBI_ERR_NOT_CONVERGED) at this many sweeps; default 1<<22 */
@@ -337,6 +343,12 @@ int jacobi_adapt_next(jacobi_adapt_state_t *st, double rho, double ms);
 /* Division the handle's kernels use: 1 = verified fixed-divisor division,
  * 0 = IEEE division, < 0 = error (NULL handle). */
 int jacobi_division_mode(const jacobi_handle_t *h);
+
+/* The tile the handle's tiled kernel uses (the default resolved), into
+ * *tile_x, *tile_y (host ints); 0 x 0 for SYNC. For EXACT_TEMPORAL_BLOCKED,
+ * tile_y = 0 is the column-streamed kernel (see jacobi_config_t). Returns
+ * JACOBI_OK or JACOBI_ERR_INVALID_ARG (NULL argument). */
+int jacobi_tile(const jacobi_handle_t *h, int *tile_x, int *tile_y);
 
 /*
  * Bounds-checked build. The pages have no counterpart for these calls; they

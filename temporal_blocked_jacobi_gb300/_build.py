@@ -24,7 +24,8 @@ BUILD_CHECKED = os.path.join(PKG, "_build_checked")
 LIB_CHECKED = os.path.join(PKG, "libtbjacobi_checked.so")
 # The four kernels_etb_part*.cu units come first: they take longest.
 SOURCES = ["kernels_etb_part0.cu", "kernels_etb_part1.cu", "kernels_etb_part2.cu",
-           "kernels_etb_part3.cu", "kernels_etb.cu", "kernels_sync.cu",
+           "kernels_etb_part3.cu", "kernels_etb.cu", "kernels_etbs.cu",
+           "kernels_sync.cu",
            "kernels_tiled.cu", "kernels_ba.cu", "kernels_bar.cu", "fastdiv.cu",
            "jacobi_abi.cu", "residual_noalloc.cu", "adapt.cu"]
 HEADERS = [os.path.join(CSRC, "jacobi_kernels.cuh"),

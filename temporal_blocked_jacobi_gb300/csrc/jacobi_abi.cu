@@ -36,6 +36,7 @@ struct jacobi_handle {
     // Tiled strategies.
     TileConf tc{};
     CUtensorMap map_u{}, map_alt{}, map_b{};
+    int *etbs_work = nullptr;  // column-streamed ETB: its work list (device)
 
     // Sweeps per launch, launches per check, sweeps per check.
     int per_launch = 1;
@@ -258,8 +259,8 @@ cudaError_t enqueue_launch(jacobi_handle_t *h, int src_is_alt,
         case JACOBI_SYNC:
             return launch_sweep_sync(h->g, src, h->b, dst, ctl, s);
         case JACOBI_EXACT_TEMPORAL_BLOCKED:
-            return launch_sweep_etb(h->g, h->tc, map_src, &h->map_b, dst,
-                                    h->dev_out, ctl, s);
+            return launch_sweep_etb(h->g, h->tc, map_src, &h->map_b, src,
+                                    h->b, dst, h->dev_out, ctl, s);
         default:
             return launch_sweep_ba(h->g, h->tc, map_src, &h->map_b, src,
                                    h->b, dst, h->dev_out, ctl, s);
@@ -666,6 +667,26 @@ int fast_division_ok(jacobi_handle_t *h, bool *ok) {
     return JACOBI_OK;
 }
 
+// Column-streamed exact temporal blocking: the device work list of the
+// prepared shape (counters at zero, then the row bands).
+int setup_etbs_work(jacobi_handle_t *h) {
+    if (h->etbs_work) {
+        cudaFree(h->etbs_work);
+        h->etbs_work = nullptr;
+    }
+    std::vector<int> list(2 + (size_t)h->g.n + 1, 0);
+    const int ints = etbs_schedule(h->tc, h->g.n, list.data() + 2,
+                                   (int)list.size() - 2);
+    if (ints < 3)
+        return fail(h, JACOBI_ERR_CUDA, "no work list for the streamed kernel");
+    TBJ_CUDA(h, cudaMalloc(&h->etbs_work, sizeof(int) * ints));
+    TBJ_CUDA(h, cudaMemcpy(h->etbs_work, list.data(), sizeof(int) * ints,
+                           cudaMemcpyHostToDevice));
+    h->tc.work = h->etbs_work;
+    h->tc.bands = ints - 3;
+    return JACOBI_OK;
+}
+
 // Apply a (validated) configuration: tiles, tensor maps, graphs.
 int create_levels(jacobi_handle_t *h, const jacobi_config_t &c);
 
@@ -694,7 +715,8 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
     }
     int rc = 0;
     if (c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED)
-        rc = etb_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc);
+        rc = etb_configure(h->g.n, c.depth, c.tile_x, c.tile_y, &h->tc,
+                           c.control != JACOBI_CONTROL_PERSISTENT);
     else if (c.strategy == JACOBI_BLOCK_ASYNC)
         rc = ba_configure(h->g.n, c.depth, c.tile_x, c.tile_y, c.overlap_x,
                           c.overlap_y, &h->tc);
@@ -716,6 +738,9 @@ int apply_config(jacobi_handle_t *h, const jacobi_config_t &c) {
         TBJ_CUDA(h, c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED
                         ? prepare_sweep_etb(h->tc, h->g.n)
                         : prepare_sweep_ba(h->tc));
+        if (c.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED &&
+            h->tc.variant == kEtbsVariant && (rc = setup_etbs_work(h)))
+            return rc;
     }
     if (c.control == JACOBI_CONTROL_PERSISTENT) {
         if (!etb_persistent_ok(h->tc))
@@ -1212,12 +1237,21 @@ void jacobi_destroy(jacobi_handle_t *h) {
     for (auto &e : h->ev)
         if (e) cudaEventDestroy(e);
     if (h->capture) cudaStreamDestroy(h->capture);
+    if (h->etbs_work) cudaFree(h->etbs_work);
     if (h->dev_out) cudaFree(h->dev_out);
     if (h->host_out) cudaFreeHost(h->host_out);
     if (h->loop) cudaFree(h->loop);
     if (h->loop_host) cudaFreeHost(h->loop_host);
     if (h->g_copy) cudaFree(h->g_copy);
     delete h;
+}
+
+int jacobi_tile(const jacobi_handle_t *h, int *tile_x, int *tile_y) {
+    if (!h || !tile_x || !tile_y) return JACOBI_ERR_INVALID_ARG;
+    const bool tiled = h->cfg.strategy != JACOBI_SYNC;
+    *tile_x = tiled ? h->tc.tile_x : 0;
+    *tile_y = tiled ? h->tc.tile_y : 0;
+    return JACOBI_OK;
 }
 
 int jacobi_bounds_checked(void) { return kBoundsChecked ? 1 : 0; }

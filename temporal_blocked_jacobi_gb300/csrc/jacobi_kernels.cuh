@@ -559,20 +559,48 @@ struct TileConf {
     int stream, ch, sx, sy, grid_x, grid_y;
     // Block-asynchronous overlapping subdomains (generic kernel only).
     int overlap_x, overlap_y;
+    // Column-streamed exact temporal blocking: the handle's work list
+    // (device: [0] next run, [1] warps done, [2 ..] band start rows) and its
+    // number of row bands.
+    int *work;
+    int bands;
 };
 
 // Exact temporal blocking (section 02 "Exact temporal blocking", after Meng
 // and Skadron): halo D deep, valid region shrinking by one cell per sweep.
-int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc);
+// streamed: whether the default tile may be the column-streamed kernel
+// (not under persistent control, which needs a register-band shape).
+int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc,
+                  bool streamed = true);
 // Raise the kernel's dynamic shared memory limit; call before any launch or
 // graph capture that uses `tc`.
 // (also sizes the persistent grid, tc.ctas)
 cudaError_t prepare_sweep_etb(TileConf &tc, int n);
+// src / b: the launch's input iterate and the right-hand side (raw
+// pointers, for the column-streamed kernel; the others use the maps).
 cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              const CUtensorMap *map_src,
-                             const CUtensorMap *map_b, float *out,
-                             ResidualOut *status, const LaunchCtl &ctl,
-                             cudaStream_t stream);
+                             const CUtensorMap *map_b, const float *src,
+                             const float *b, float *out, ResidualOut *status,
+                             const LaunchCtl &ctl, cudaStream_t stream);
+
+// Column-streamed exact temporal blocking (kernels_etbs.cu): selected with
+// tile_x = 128 - 2 * round_up(D, 4) and tile_y = 0, TileConf::variant =
+// kEtbsVariant. D = 8 only.
+constexpr int kEtbsVariant = 1000;
+bool etbs_configure(int n, int depth, TileConf *tc);
+cudaError_t prepare_sweep_etbs(TileConf &tc, int n);
+// Host: the work list's row bands for `tc` (prepared) on an n x n grid:
+// band_start receives bands + 1 row numbers, from 1 to n - 1. Returns the
+// number of ints the device work list needs (2 + bands + 1).
+int etbs_schedule(const TileConf &tc, int n, int *band_start, int cap);
+// Whether the column-streamed kernel is the better D = 8 kernel for this
+// grid on `sms` SMs (enough output rows per warp to amortise the pipeline).
+bool etbs_preferred(int n, int sms);
+cudaError_t launch_sweep_etbs(const GridDesc &g, const TileConf &tc,
+                              const float *src, const float *b, float *out,
+                              unsigned *err, const LaunchCtl &ctl,
+                              cudaStream_t stream);
 
 // Persistent exact temporal blocking (JACOBI_CONTROL_PERSISTENT): one
 // cooperative launch runs a whole time step. `tc` must be a register-resident

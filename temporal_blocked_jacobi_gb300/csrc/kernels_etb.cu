@@ -42,8 +42,22 @@ int etb_default_variant(int n, int depth) {
 
 }  // namespace
 
-int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
+int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc,
+                  bool streamed) {
     if (depth != 2 && depth != 4 && depth != 8 && depth != 16) return -1;
+    // Whole columns: the column-streamed kernel (kernels_etbs.cu), also the
+    // default at D = 8 on grids with enough rows per warp.
+    if (tile_y == 0 && tile_x == 128 - 2 * ((depth + 3) / 4 * 4))
+        return etbs_configure(n, depth, tc) ? 0 : -5;
+    if (streamed && tile_x == 0 && tile_y == 0 && depth == 8) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+                cudaSuccess &&
+            sms > 0 && etbs_preferred(n, sms))
+            return etbs_configure(n, depth, tc) ? 0 : -5;
+        cudaGetLastError();
+    }
     int pick = tile_x == 0 && tile_y == 0 ? etb_default_variant(n, depth) : -1;
     for (int v = 0; v < (int)(sizeof(kVariants) / sizeof(kVariants[0])); ++v) {
         const EtbVariant &k = kVariants[v];
@@ -71,6 +85,8 @@ int etb_configure(int n, int depth, int tile_x, int tile_y, TileConf *tc) {
     tc->variant = pick;
     tc->ctas = 0;  // set by prepare_sweep_etb
     tc->stream = tc->ch = tc->sx = tc->sy = tc->grid_x = tc->grid_y = 0;
+    tc->work = nullptr;
+    tc->bands = 0;
     return 0;
 }
 
@@ -83,6 +99,7 @@ bool valid_variant(int v) {
 }  // namespace
 
 cudaError_t prepare_sweep_etb(TileConf &tc, int n) {
+    if (tc.variant == kEtbsVariant) return prepare_sweep_etbs(tc, n);
     if (!valid_variant(tc.variant)) return cudaErrorInvalidValue;
     switch (kVariantPart[tc.variant]) {
         case 0: return etb_part0_prepare(tc.variant, tc, n);
@@ -132,11 +149,13 @@ cudaError_t launch_etb_persistent(const GridDesc &g, const TileConf &tc,
 
 cudaError_t launch_sweep_etb(const GridDesc &g, const TileConf &tc,
                              const CUtensorMap *map_src,
-                             const CUtensorMap *map_b, float *out,
-                             ResidualOut *status, const LaunchCtl &ctl,
-                             cudaStream_t stream) {
-    if (!valid_variant(tc.variant)) return cudaErrorInvalidValue;
+                             const CUtensorMap *map_b, const float *src,
+                             const float *b, float *out, ResidualOut *status,
+                             const LaunchCtl &ctl, cudaStream_t stream) {
     unsigned *err = ctl.lp.state ? &ctl.lp.state->err : &status->err;
+    if (tc.variant == kEtbsVariant)
+        return launch_sweep_etbs(g, tc, src, b, out, err, ctl, stream);
+    if (!valid_variant(tc.variant)) return cudaErrorInvalidValue;
 #define TBJ_P(P)                                                          \
     case P:                                                               \
         return etb_part##P##_launch(tc.variant, g, tc, map_src, map_b, out, \

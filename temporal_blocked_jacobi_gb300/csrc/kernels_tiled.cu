@@ -318,6 +318,8 @@ int ba_configure(int n, int depth, int tile_x, int tile_y, int overlap_x,
     tc->variant = 0;
     tc->ctas = 0;
     tc->stream = tc->ch = tc->sx = tc->sy = 0;
+    tc->work = nullptr;
+    tc->bands = 0;
     tc->grid_x = subdomain_count(n - 2, tile_x, overlap_x);
     tc->grid_y = subdomain_count(n - 2, tile_y, overlap_y);
     // Non-overlapping 32 x 8 tiles (the default) are held in registers; the

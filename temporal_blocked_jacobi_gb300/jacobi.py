@@ -104,6 +104,7 @@ def load(checked: bool = False):
             "jacobi_adapt_init": (i, [ctypes.POINTER(AdaptState), i, i]),
             "jacobi_adapt_next": (i, [ctypes.POINTER(AdaptState), ctypes.c_double,
                                       ctypes.c_double]),
+            "jacobi_tile": (i, [vp, ctypes.POINTER(i), ctypes.POINTER(i)]),
             "jacobi_bounds_checked": (i, []),
             "jacobi_bounds_selftest": (i, [vp]),
         }
@@ -314,6 +315,15 @@ class Solver:
     def division_mode(self) -> int:
         """1 if the kernels use the verified fixed-divisor division, 0 if IEEE."""
         return int(self._ok(self._lib.jacobi_division_mode(self.handle)))
+
+    @property
+    def tile(self):
+        """(tile_x, tile_y) of the handle's tiled kernel, the default
+        resolved; (0, 0) for SYNC; tile_y = 0 is the column-streamed
+        exact-temporal-blocking kernel."""
+        tx, ty = ctypes.c_int(), ctypes.c_int()
+        self._ok(self._lib.jacobi_tile(self.handle, ctypes.byref(tx), ctypes.byref(ty)))
+        return tx.value, ty.value
 
     @property
     def launch_count(self) -> int:

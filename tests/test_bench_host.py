@@ -157,3 +157,11 @@ def test_gpus_flag_must_match_the_launcher():
         capture_output=True, text=True, timeout=120, cwd=ROOT,
         env={**os.environ, "WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
     assert res.returncode != 0 and "WORLD_SIZE" in res.stderr
+
+
+def test_kernel_name_follows_the_resolved_tile():
+    """tile_y = 0 is the column-streamed kernel (the D = 8 default on large
+    grids); the solver reports the tile it resolved."""
+    assert bench.kernel_name("etb8", (112, 0)).startswith("k_etbs")
+    assert bench.kernel_name("etb8@112x0").startswith("k_etbs")
+    assert bench.kernel_name("etb8", (112, 92)).startswith("k_etbr")

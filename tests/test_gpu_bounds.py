@@ -53,7 +53,7 @@ def test_checker_refuses_out_of_range_accesses():
 ETB = [(2, (0, 0)), (4, (0, 0)), (8, (0, 0)), (16, (0, 0)),
        (2, (120, 60)), (2, (248, 60)), (2, (120, 92)), (4, (120, 56)),
        (4, (248, 56)), (4, (120, 40)), (4, (120, 88)), (8, (112, 80)),
-       (8, (112, 48)), (8, (112, 112)), (8, (240, 48)), (8, (112, 92)),
+       (8, (112, 48)), (8, (112, 112)), (8, (240, 48)), (8, (112, 92)), (8, (112, 0)),
        (16, (96, 64)), (16, (96, 96)), (16, (224, 64)), (16, (96, 76))]
 
 

@@ -111,3 +111,22 @@ def test_n8192_first_interval_every_strategy():
     from tests.test_gpu_solve import first_interval_matches_oracle
     for strategy, depth in (("sync", 1), ("etb", 4), ("etb", 8), ("etb", 16)):
         first_interval_matches_oracle(8192, 100.0, "gauss", strategy, depth)
+
+
+def test_default_d8_kernel_follows_the_grid():
+    """At D = 8 the default is the column-streamed kernel (tile 112 x 0) on
+    grids with enough rows per warp and a register-band shape on small ones;
+    persistent control always gets a register-band shape."""
+    import torch
+    from temporal_blocked_jacobi_gb300 import jacobi
+    for n, want in ((2048, (112, 92)), (8192, (112, 0)), (18432, (112, 0))):
+        u, u_alt, b = jacobi.allocate(n)
+        with jacobi.Solver(u, u_alt, b, 10.0, strategy="etb", depth=8,
+                           control="device") as s:
+            assert s.tile == want, (n, s.tile)
+        if n == 8192:
+            with jacobi.Solver(u, u_alt, b, 10.0, strategy="etb", depth=8,
+                               control="persistent") as s:
+                assert s.tile[1] > 0
+        del u, u_alt, b
+        torch.cuda.empty_cache()

@@ -100,7 +100,8 @@ def test_unfused_rhs_sweep_residual(n, pad, division):
 # ((0, 0) selects the default).
 ETB_TILES = {2: [(0, 0), (120, 60), (248, 60)],
              4: [(0, 0), (120, 56), (248, 56), (120, 40)],
-             8: [(0, 0), (112, 80), (112, 48), (112, 112), (240, 48), (112, 92)],
+             8: [(0, 0), (112, 80), (112, 48), (112, 112), (240, 48), (112, 92),
+                 (112, 0)],  # (112, 0): whole columns, streamed (k_etbs)
              16: [(0, 0), (96, 64), (96, 96), (224, 64), (96, 76)]}
 ETB_CASES = [(dd, t) for dd, ts in ETB_TILES.items() for t in ts]
 
