@@ -292,6 +292,31 @@ long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
                      long long *sweeps_per_step);
 
 /*
+ * Independent problems on host data (the time-step loop of section 01 for
+ * each of `count` problems of the handle's size, r and configuration):
+ * problem i starts from u0_host[i] (host, N*ld floats with its Dirichlet
+ * ring), has source g_host[i] (host, N*ld floats) and runs `steps` time
+ * steps as jacobi_run does; its final field is written to u_host[i] (host,
+ * N*ld floats). sweeps (host, count * steps entries, may be NULL) receives
+ * the sweeps of every step, problem by problem. Returns the total sweep
+ * count or the first negative status (later problems are not run).
+ *
+ * The host-device copies overlap the solves: problem i + 1's inputs are
+ * copied in, and problem i - 1's result out, while problem i is solved, on
+ * a stream of the handle's own. Host buffers should be pinned
+ * (cudaHostAlloc or equivalent) for the copies to be asynchronous. u, u_alt
+ * are overwritten (u holds the last problem's result on return), and b
+ * receives the right-hand sides. On first use the handle allocates four
+ * device buffers of N*ld floats (staging for the copies), a stream and four
+ * events, kept until jacobi_destroy. Synchronous: returns when every result
+ * is in host memory.
+ */
+long long jacobi_run_host(jacobi_handle_t *h, int count,
+                          const float *const *u0_host,
+                          const float *const *g_host, float *const *u_host,
+                          int steps, long long *sweeps);
+
+/*
  * One residual check of the last jacobi_solve_step, in order. depth: D of the
  * launches of that check interval; sweeps: sweeps done when the check was
  * taken; rmax, bmax: its norms; ms: device time of the interval (its launches

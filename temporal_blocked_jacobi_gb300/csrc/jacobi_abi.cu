@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <new>
@@ -37,6 +38,15 @@ struct jacobi_handle {
     TileConf tc{};
     CUtensorMap map_u{}, map_alt{}, map_b{};
     int *etbs_work = nullptr;  // column-streamed ETB: its work list (device)
+
+    // Host-buffer runs (jacobi_run_host), allocated on first use: the next
+    // problem's u0 and g staged on the device, the g of the problem being
+    // solved, the last result on its way out, and a stream for the copies.
+    float *hb_u = nullptr, *hb_g = nullptr, *hb_gdev = nullptr, *hb_out = nullptr;
+    cudaStream_t hb_copy = nullptr;
+    // inputs staged, inputs taken, result staged, result copied out
+    cudaEvent_t hb_staged = nullptr, hb_taken = nullptr, hb_result = nullptr,
+                hb_copied = nullptr;
 
     // Sweeps per launch, launches per check, sweeps per check.
     int per_launch = 1;
@@ -1243,7 +1253,83 @@ void jacobi_destroy(jacobi_handle_t *h) {
     if (h->loop) cudaFree(h->loop);
     if (h->loop_host) cudaFreeHost(h->loop_host);
     if (h->g_copy) cudaFree(h->g_copy);
+    if (h->hb_copy) cudaStreamSynchronize(h->hb_copy);
+    for (float *p : {h->hb_u, h->hb_g, h->hb_gdev, h->hb_out})
+        if (p) cudaFree(p);
+    for (cudaEvent_t e : {h->hb_staged, h->hb_taken, h->hb_result, h->hb_copied})
+        if (e) cudaEventDestroy(e);
+    if (h->hb_copy) cudaStreamDestroy(h->hb_copy);
     delete h;
+}
+
+long long jacobi_run_host(jacobi_handle_t *h, int count,
+                          const float *const *u0_host,
+                          const float *const *g_host, float *const *u_host,
+                          int steps, long long *sweeps) {
+    if (!h) return JACOBI_ERR_INVALID_ARG;
+    if (count < 1 || steps < 1 || !u0_host || !g_host || !u_host)
+        return fail(h, JACOBI_ERR_INVALID_ARG,
+                    "count and steps must be >= 1 and the pointer arrays non-NULL");
+    for (int i = 0; i < count; ++i)
+        if (!u0_host[i] || !g_host[i] || !u_host[i])
+            return fail(h, JACOBI_ERR_INVALID_ARG, "problem %d has a NULL buffer", i);
+    const size_t bytes = sizeof(float) * (size_t)h->g.n * (size_t)h->g.ld;
+    if (!h->hb_copy) {  // first use: device staging, copy stream, events
+        TBJ_CUDA(h, cudaMalloc(&h->hb_u, bytes));
+        TBJ_CUDA(h, cudaMalloc(&h->hb_g, bytes));
+        TBJ_CUDA(h, cudaMalloc(&h->hb_gdev, bytes));
+        TBJ_CUDA(h, cudaMalloc(&h->hb_out, bytes));
+        for (cudaEvent_t *e : {&h->hb_staged, &h->hb_taken, &h->hb_result, &h->hb_copied})
+            TBJ_CUDA(h, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+        TBJ_CUDA(h, cudaStreamCreateWithFlags(&h->hb_copy, cudaStreamNonBlocking));
+    }
+    cudaStream_t cs = h->hb_copy;
+    // The copy stream starts after everything already queued on the handle's
+    // stream (the caller may have been using the buffers).
+    TBJ_CUDA(h, cudaEventRecord(h->hb_result, h->stream));
+    TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_result, 0));
+    TBJ_CUDA(h, cudaEventRecord(h->hb_copied, cs));
+    TBJ_CUDA(h, cudaMemcpyAsync(h->hb_u, u0_host[0], bytes, cudaMemcpyHostToDevice, cs));
+    TBJ_CUDA(h, cudaMemcpyAsync(h->hb_g, g_host[0], bytes, cudaMemcpyHostToDevice, cs));
+    TBJ_CUDA(h, cudaEventRecord(h->hb_staged, cs));
+    long long total = 0, status = 0;
+    for (int i = 0; i < count; ++i) {
+        // Take problem i's inputs: u0 into u (and u_alt, whose Dirichlet ring
+        // must equal u's), g into the buffer the solve reads.
+        TBJ_CUDA(h, cudaStreamWaitEvent(h->stream, h->hb_staged, 0));
+        TBJ_CUDA(h, cudaMemcpyAsync(h->u, h->hb_u, bytes, cudaMemcpyDeviceToDevice, h->stream));
+        TBJ_CUDA(h, cudaMemcpyAsync(h->u_alt, h->hb_u, bytes, cudaMemcpyDeviceToDevice, h->stream));
+        TBJ_CUDA(h, cudaMemcpyAsync(h->hb_gdev, h->hb_g, bytes, cudaMemcpyDeviceToDevice, h->stream));
+        TBJ_CUDA(h, cudaEventRecord(h->hb_taken, h->stream));
+        h->cur = 0;
+        // Stage problem i + 1's inputs while problem i is solved.
+        if (i + 1 < count) {
+            TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_taken, 0));
+            TBJ_CUDA(h, cudaMemcpyAsync(h->hb_u, u0_host[i + 1], bytes,
+                                        cudaMemcpyHostToDevice, cs));
+            TBJ_CUDA(h, cudaMemcpyAsync(h->hb_g, g_host[i + 1], bytes,
+                                        cudaMemcpyHostToDevice, cs));
+            TBJ_CUDA(h, cudaEventRecord(h->hb_staged, cs));
+        }
+        const long long k = jacobi_run(h, h->hb_gdev, steps,
+                                       sweeps ? sweeps + (size_t)i * steps : nullptr);
+        if (k < 0) {
+            status = k;
+            break;
+        }
+        total += k;
+        // Problem i's result: into the outgoing buffer once the previous
+        // result has left it, then to the host while problem i + 1 runs.
+        TBJ_CUDA(h, cudaStreamWaitEvent(h->stream, h->hb_copied, 0));
+        TBJ_CUDA(h, cudaMemcpyAsync(h->hb_out, h->u, bytes, cudaMemcpyDeviceToDevice, h->stream));
+        TBJ_CUDA(h, cudaEventRecord(h->hb_result, h->stream));
+        TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_result, 0));
+        TBJ_CUDA(h, cudaMemcpyAsync(u_host[i], h->hb_out, bytes, cudaMemcpyDeviceToHost, cs));
+        TBJ_CUDA(h, cudaEventRecord(h->hb_copied, cs));
+    }
+    TBJ_CUDA(h, cudaStreamSynchronize(cs));
+    TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
+    return status ? status : total;
 }
 
 int jacobi_tile(const jacobi_handle_t *h, int *tile_x, int *tile_y) {

@@ -105,6 +105,8 @@ def load(checked: bool = False):
             "jacobi_adapt_next": (i, [ctypes.POINTER(AdaptState), ctypes.c_double,
                                       ctypes.c_double]),
             "jacobi_tile": (i, [vp, ctypes.POINTER(i), ctypes.POINTER(i)]),
+            "jacobi_run_host": (ll, [vp, i, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                     ctypes.POINTER(vp), i, ctypes.POINTER(ll)]),
             "jacobi_bounds_checked": (i, []),
             "jacobi_bounds_selftest": (i, [vp]),
         }
@@ -298,6 +300,32 @@ class Solver:
         if total < 0:
             self._raise(total)
         return [int(counts[s]) for s in range(steps)]
+
+    def run_host(self, u0s, gs, outs, steps=10):
+        """jacobi_run_host: independent problems on host tensors (pinned CPU
+        float32 tensors of shape (N, ld)); problem i starts from u0s[i] with
+        source gs[i] and leaves its final field in outs[i]. The copies
+        overlap the solves. Returns the sweeps of every step, per problem."""
+        import torch
+        count = len(u0s)
+        if not (count == len(gs) == len(outs)) or count < 1:
+            raise ValueError("u0s, gs and outs must be non-empty and of one length")
+        for t in (*u0s, *gs, *outs):
+            if not (isinstance(t, torch.Tensor) and not t.is_cuda
+                    and t.dtype == torch.float32 and t.is_contiguous()
+                    and tuple(t.shape) == (self.n, self.ld)):
+                raise ValueError("host buffers must be contiguous float32 CPU "
+                                 f"tensors of shape {(self.n, self.ld)}")
+        arr = ctypes.c_void_p * count
+        pu = arr(*[t.data_ptr() for t in u0s])
+        pg = arr(*[t.data_ptr() for t in gs])
+        po = arr(*[t.data_ptr() for t in outs])
+        counts = (ctypes.c_longlong * (count * steps))()
+        total = self._lib.jacobi_run_host(self.handle, count, pu, pg, po, int(steps),
+                                          counts)
+        if total < 0:
+            self._raise(total)
+        return [[int(counts[i * steps + s]) for s in range(steps)] for i in range(count)]
 
     def check_trace(self):
         """The last solve_step's checks: list of dicts (depth, sweeps, rmax,

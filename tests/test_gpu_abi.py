@@ -3,8 +3,9 @@ non-finite residuals are reported, and the handle stays usable after."""
 import numpy as np
 import pytest
 
+import oracle
 from temporal_blocked_jacobi_gb300 import problem as P
-from tests.gpu_helpers import to_dev, workload
+from tests.gpu_helpers import mismatch, same_bits, to_dev, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -262,3 +263,36 @@ def test_device_control_launch_count(strategy, depth):
         iters = -(-checks // body)
         copy = 1 if (L % 2 and checks % 2 == 0) else 0
         assert s.launch_count - c0 == 2 + iters * (body * L + 1) + copy
+
+
+def test_run_host_matches_the_oracle_problem_by_problem():
+    """jacobi_run_host: independent problems given as host buffers, each
+    equal to the oracle's ten-step solve of its own inputs (different
+    sources and boundary rows), whatever the copies' overlap; pinned and
+    pageable host memory."""
+    import torch
+    from temporal_blocked_jacobi_gb300 import jacobi
+    n, r, steps = 130, 10.0, 3
+    ld = P.padded_ld(n)
+    cases = []
+    for k, (src, top) in enumerate((("point", 100.0), ("gauss", 50.0),
+                                    ("gauss", 100.0), ("point", 0.0))):
+        u0 = P.initial_field(n, ld, top=top)
+        g = P.source_term(n, ld, src, amplitude=1000.0 * (k + 1) if src == "point" else None)
+        cases.append((u0, g, *oracle.run(u0, g, r, steps=steps)[:2]))
+    for pinned in (True, False):
+        for kw in ({"strategy": "etb", "depth": 8, "control": "device"},
+                   {"strategy": "sync", "control": "host"}):
+            u, u_alt, b = jacobi.allocate(n, ld)
+            u0s = [torch.from_numpy(c[0]) for c in cases]
+            gs = [torch.from_numpy(c[1]) for c in cases]
+            outs = [torch.full((n, ld), float("nan")) for _ in cases]
+            if pinned:
+                u0s = [t.pin_memory() for t in u0s]
+                gs = [t.pin_memory() for t in gs]
+                outs = [t.pin_memory() for t in outs]
+            with jacobi.Solver(u, u_alt, b, r, **kw) as s:
+                counts = s.run_host(u0s, gs, outs, steps)
+            for (u0, g, ref_u, ref_k), got, k in zip(cases, outs, counts):
+                assert k == ref_k, (kw, pinned, k, ref_k)
+                assert same_bits(got.numpy()[:, :n], ref_u[:, :n]), (kw, pinned, mismatch(got.numpy(), ref_u))
