@@ -143,10 +143,11 @@ enum : unsigned {
 // Bounds-checked build.
 //
 // Compiled with JACOBI_BOUNDS_CHECK (libtbjacobi_checked.so, a testing aid
-// standing in for a memory checker), the tiled kernels -- k_etbr, k_etb,
-// k_bar, k_ba, k_block_async -- route every shared-memory access, every
-// plain global load of a grid and every global store through the accessors
-// below, and check every TMA box load's x coordinate and destination. An
+// standing in for a memory checker), the tiled kernels -- k_etbs, k_etbr,
+// k_etb, k_etbp, k_bar, k_ba, k_block_async -- route every shared-memory
+// access, every plain global load of a grid and every global store through
+// the accessors below, and check every TMA box load's x coordinate and
+// destination. An
 // access outside its range is not performed: it sets ERR_BOUNDS in the
 // launch's error word (reported as JACOBI_ERR_CUDA) and a load yields NaN.
 // Nothing traps. The ranges are
