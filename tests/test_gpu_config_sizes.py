@@ -12,8 +12,9 @@ interval or through GPU self-consistency.
   the GPU's, which is bit-exact to the oracle (below and in
   test_gpu_solve.py).
 * Ten full time steps of SYNC and EXACT_TEMPORAL_BLOCKED(8) at N = 4096
-  (r = 1 and 10) against the oracle run on all host cores (row-parallel, bit
-  for bit equal to the single-threaded oracle: test_oracle_threads.py).
+  (r = 1 and 10) and at N = 18432 (r = 10, point source) against the oracle
+  run on all host cores (row-parallel, bit for bit equal to the
+  single-threaded oracle: test_oracle_threads.py).
 * The first check interval at N = 8192, r = 100 for SYNC and
   EXACT_TEMPORAL_BLOCKED with D = 4, 8 and 16 (D = 16: one 16-sweep launch).
 """
@@ -130,3 +131,19 @@ def test_default_d8_kernel_follows_the_grid():
                 assert s.tile[1] > 0
         del u, u_alt, b
         torch.cuda.empty_cache()
+
+
+def test_n18432_ten_steps_bit_exact_to_threaded_oracle():
+    """The default bench configuration (N = 18432, r = 10, point source):
+    all ten time steps of SYNC and of EXACT_TEMPORAL_BLOCKED(8) (the
+    column-streamed kernel at this N) against the oracle run on all host
+    cores, fields and sweep counts bit for bit. About 8e11 lattice updates
+    on the host."""
+    u0, g = workload(18432, "point")
+    ref_u, ref_k, _ = oracle.run(u0, g, 10.0, threads=host_threads())
+    for kw in ({"strategy": "etb", "depth": 8, "control": "device"},
+               {"strategy": "sync", "depth": 1, "control": "device"}):
+        got_u, got_k, _ = gpu_run(u0, g, 10.0, **kw)
+        assert got_k == ref_k, (kw, got_k, ref_k)
+        assert same_bits(got_u, ref_u), (kw, mismatch(got_u, ref_u))
+        del got_u
