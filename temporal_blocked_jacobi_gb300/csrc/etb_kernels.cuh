@@ -164,7 +164,7 @@ __device__ __forceinline__ void etb_sweep(const float *src, float *dst, int s,
         for (int c = 0; c < CH; ++c) {
             const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
             const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
-            float4 nv = update4_we<FAST>(nr[c], cr[c], sr[c], breg[j][c], w, e, r,
+            float4 nv = update4_we<FAST, false>(nr[c], cr[c], sr[c], breg[j][c], w, e, r,
                                       d, y);
             if (RESID) {
                 const bool tile_row = row >= D && row < D + S::TY;
@@ -439,7 +439,7 @@ __device__ __forceinline__ void etbr_row(int j, float4 (&u)[RW][CH],
         const float w = (c > 0 && lane == 0) ? wv[c - 1] : wv[c];
         const float e = (c < CH - 1 && lane == 31) ? ev[c + 1] : ev[c];
         const float4 cur = u[j][c];
-        float4 nv = update4_we<FAST>(north[c], cur, south[c], b[j][c], w, e, r,
+        float4 nv = update4_we<FAST, false>(north[c], cur, south[c], b[j][c], w, e, r,
                                      d, y);
         if (RESID) {
             const bool tile_row = row >= D && row < D + S::TY;

@@ -74,7 +74,12 @@ __device__ __forceinline__ float jacobi_update(float uw, float ue, float un,
 // ---------------------------------------------------------------------------
 // J for the four cells of a float4 chunk: n4, c4, s4 the rows above, at and
 // below, w/e the cells west of .x and east of .w.
-template <bool FAST>
+// PACKDIV: the division's three steps on pairs of cells (packed) or one
+// cell at a time; the results are the same bits. Which is faster depends on
+// the kernel's instruction mix (measured on GB300: packed for the
+// column-streamed kernel, 3.5 % slower per launch with scalar division;
+// scalar for the register-band and block-async kernels, 2-6 % faster).
+template <bool FAST, bool PACKDIV = true>
 __device__ __forceinline__ float4 update4_we(float4 n4, float4 c4, float4 s4,
                                              float4 b4, float w, float e,
                                              float r, float d, float y) {
@@ -84,6 +89,9 @@ __device__ __forceinline__ float4 update4_we(float4 n4, float4 c4, float4 s4,
         // product r * s is formed with scalar round-to-nearest multiplies:
         // a packed multiply feeding a packed add can be fused into one
         // multiply-add by the compiler, which would change the rounding.
+        // (Measured on GB300: the packed-multiply intrinsic, an inline
+        // mul.rn.f32x2 and a packed fma with a -0 addend all gave fields
+        // that differ from the synchronous sweep's.)
         const float2 d2 = make_float2(d, d), y2 = make_float2(y, y);
         const float2 h01 = make_float2(__fadd_rn(w, c4.y), __fadd_rn(c4.x, c4.z));
         const float2 h23 = make_float2(__fadd_rn(c4.y, c4.w), __fadd_rn(c4.z, e));
@@ -94,6 +102,9 @@ __device__ __forceinline__ float4 update4_we(float4 n4, float4 c4, float4 s4,
         const float2 rs23 = make_float2(__fmul_rn(r, s23.x), __fmul_rn(r, s23.y));
         const float2 num01 = __fadd2_rn(make_float2(b4.x, b4.y), rs01);
         const float2 num23 = __fadd2_rn(make_float2(b4.z, b4.w), rs23);
+        if (!PACKDIV)
+            return make_float4(div_fixed(num01.x, d, y), div_fixed(num01.y, d, y),
+                               div_fixed(num23.x, d, y), div_fixed(num23.y, d, y));
         const float2 q01 = div2_fixed(num01, d2, y2);
         const float2 q23 = div2_fixed(num23, d2, y2);
         return make_float4(q01.x, q01.y, q23.x, q23.y);

@@ -153,7 +153,7 @@ __device__ __forceinline__ void bar_strip(const float *__restrict__ src,
             const float w = tile_w ? fw[j] : wv;
             const float e = tile_e ? fe[j] : ev;
             const float4 b4 = lds4(sbl + 128 * j);
-            float4 nv = update4_we<FAST>(prev, c, s4, b4, w, e, r, d, y);
+            float4 nv = update4_we<FAST, false>(prev, c, s4, b4, w, e, r, d, y);
             const bool row_ok = !EDGE || gy0 + j <= n - 2;
             if (RESID && row_ok) {
                 const float2 d01 = __fadd2_rn(make_float2(nv.x, nv.y),

@@ -124,9 +124,13 @@ __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
     int row = ra;  // next row to stage
     const float *pu = src + (long long)ra * ld + c0;
     const float *pb = bsrc + (long long)ra * ld + c0;
+    float *po = out + (long long)(ra - D) * ld + c0;  // output row ra + t - D
 
     auto issue = [&](int t) {  // stage input row ra + t (== row)
-        const bool in = col_in && row >= 0 && row < n;
+        // Interior runs stage rows and columns that all exist (the caller
+        // keeps kAhead rows of margin below them), so their copies need no
+        // test; edge runs zero-fill what lies outside the array.
+        const bool in = !EDGE || (col_in && row >= 0 && row < n);
         cp16(uown + (t & (kURing - 1)) * 128, src, pu, in);
         float *bs = bown + (t & (kRing - 1)) * 128;
         cp16(bs, bsrc, pb, in);
@@ -184,7 +188,7 @@ __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
                 if (colmask & 8u) rmf = max_nan_abs(rmf, d23.y);
             }
             if (k == D && in_tile && out_row && row_ok && colmask) {
-                float *g = out + (long long)i * ld + c0;
+                float *g = po;
                 if (colmask == 0xfu) {
                     gst4(g, nv);
                 } else {
@@ -198,6 +202,7 @@ __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
             wb[k - 1] = fresh;
             fresh = nv;
         }
+        po += ld;
     }
     cp_wait<0>();  // the rows staged past the run, before the slots are reused
 }
@@ -229,8 +234,10 @@ k_etbs(const float *__restrict__ src, const float *__restrict__ bsrc,
         const int band = (int)(c / (unsigned)strips);
         const int ya = band_start[band], yb = band_start[band + 1];
         const int bxo = s * S::TX - S::HX;
+        // Interior runs: every cell of the strip's box is an interior grid
+        // cell and the kAhead rows staged past the run exist.
         const bool edge = bxo < 1 || bxo + 128 > n - 1 || ya - D < 1 ||
-                          yb + D > n - 1;
+                          yb + D + kAhead > n;
         if (edge)
             etbs_run<D, FAST, true, FUSED>(src, bsrc, out, sw, n, ld, r, d, y,
                                            bxo, ya, yb, rmf);
