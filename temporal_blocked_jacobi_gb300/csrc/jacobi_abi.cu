@@ -65,6 +65,9 @@ struct jacobi_handle {
     LoopState *run_states = nullptr;       // device, run_cap entries
     LoopState *run_states_host = nullptr;  // pinned copy
     int run_cap = 0;
+    // The run graph's steps start with a sweep launch that forms b itself
+    // (rhs_first_launch) instead of k_rhs and k_bnorm.
+    bool run_rhs_first = false;
     int cur = 0;  // 0: the iterate is in u; 1: in u_alt
 
     // Adaptive depth (BLOCK_ASYNC with a depth controller): one fixed-depth
@@ -350,10 +353,10 @@ long long intervals_per_iteration(long long launches_per_check, int n) {
 // starting from u, each with a fused first launch and the rest honouring the
 // stop flag, then the kernel that ends the loop once the step has stopped.
 cudaError_t capture_body(jacobi_handle_t *h, LoopState *st,
-                         cudaGraphConditionalHandle cond) {
+                         cudaGraphConditionalHandle cond, int start = 0) {
     const long long L = h->launches_per_check;
     const long long halves = intervals_per_iteration(L, h->g.n);
-    int src = 0;
+    int src = start;
     cudaError_t e = cudaSuccess;
     for (long long half = 0; half < halves && e == cudaSuccess; ++half)
         for (long long l = 0; l < L && e == cudaSuccess; ++l) {
@@ -532,7 +535,21 @@ int record_run_persistent(jacobi_handle_t *h, const float *g, int steps) {
     return JACOBI_OK;
 }
 
+// Whether a device-controlled run starts each step with a sweep launch that
+// forms the right-hand side b = u^n + g itself (and the cells of bmax
+// without ring neighbours) from the u^n it reads, in place of k_rhs and
+// k_bnorm: the column-streamed ETB kernel, with one launch per check
+// interval (that first launch is the step's first interval, which has no
+// check: section 01, the first check comes after M sweeps).
+bool rhs_first_launch(const jacobi_handle_t *h) {
+    return h->cfg.control == JACOBI_CONTROL_DEVICE &&
+           h->cfg.rhs == JACOBI_RHS_FUSED &&
+           h->cfg.strategy == JACOBI_EXACT_TEMPORAL_BLOCKED &&
+           h->tc.variant == kEtbsVariant && h->launches_per_check == 1;
+}
+
 int record_run(jacobi_handle_t *h, const float *g, int steps) {
+    h->run_rhs_first = false;
     if (h->cfg.control == JACOBI_CONTROL_PERSISTENT)
         return record_run_persistent(h, g, steps);
     if (h->run) cudaGraphExecDestroy(h->run);
@@ -550,6 +567,7 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
         h->run_cap = steps;
     }
     const bool settle_needed = h->launches_per_check % 2 == 1;
+    const bool rhs_first = rhs_first_launch(h);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaGraphCreate(&graph, 0);
     auto check = [&](cudaError_t err) {
@@ -567,14 +585,28 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
             check(cudaStreamBeginCaptureToGraph(
                 h->capture, graph, prev ? &prev : nullptr, nullptr,
                 prev ? 1 : 0, cudaStreamCaptureModeThreadLocal))) {
-            if (h->cfg.rhs == JACOBI_RHS_UNFUSED) {
-                if (s == 0) check(launch_copy_interior(h->g, g, h->g_copy, h->capture));
-                check(launch_copy_interior(h->g, h->u, h->b, h->capture));
+            if (rhs_first) {
+                // reset (the loop starts one interval in) -> bmax of the
+                // ring-adjacent cells -> the step's first launch, u -> u_alt,
+                // which forms b and the rest of bmax.
+                check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture,
+                                        h->interval));
+                check(launch_bnorm_ring(h->g, h->u, g, st, h->capture));
+                LaunchCtl c = loop_ctl(h, st, false, 0, cond);
+                c.rhs_g = g;
+                c.rhs_b = h->b;
+                check(enqueue_launch(h, 0, h->capture, c));
             } else {
-                check(launch_rhs(h->g, h->u, g, h->b, h->capture));
+                if (h->cfg.rhs == JACOBI_RHS_UNFUSED) {
+                    if (s == 0)
+                        check(launch_copy_interior(h->g, g, h->g_copy, h->capture));
+                    check(launch_copy_interior(h->g, h->u, h->b, h->capture));
+                } else {
+                    check(launch_rhs(h->g, h->u, g, h->b, h->capture));
+                }
+                check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture));
+                check(launch_bnorm(h->g, h->u, h->b, st, h->capture));
             }
-            check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture));
-            check(launch_bnorm(h->g, h->u, h->b, st, h->capture));
             cudaStreamCaptureStatus cs;
             const cudaGraphNode_t *deps = nullptr;
             size_t ndeps = 0;
@@ -599,7 +631,7 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
         if (e == cudaSuccess &&
             check(cudaStreamBeginCaptureToGraph(h->capture, body, nullptr, nullptr,
                                                 0, cudaStreamCaptureModeThreadLocal))) {
-            check(capture_body(h, st, cond));
+            check(capture_body(h, st, cond, rhs_first ? 1 : 0));
             cudaGraph_t g2 = nullptr;
             check(cudaStreamEndCapture(h->capture, &g2));
         }
@@ -637,6 +669,7 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
         return fail(h, JACOBI_ERR_CUDA, "recording the run graph: %s",
                     cudaGetErrorString(e));
     }
+    h->run_rhs_first = rhs_first;
     h->run_g = g;
     h->run_steps = steps;
     return JACOBI_OK;
@@ -960,14 +993,19 @@ static int check_b_mode(jacobi_handle_t *h) {
 // the body (no-op launches after the stop included) and its condition
 // kernel. A skipped step runs one iteration of no-ops.
 static long long device_step_launches(const jacobi_handle_t *h,
-                                      const LoopState &st) {
+                                      const LoopState &st,
+                                      bool rhs_first = false) {
     // persistent: reset, bmax and the one cooperative launch
     if (h->cfg.control == JACOBI_CONTROL_PERSISTENT) return 3;
     const long long per_body = intervals_per_iteration(h->launches_per_check, h->g.n);
-    const long long checks =
-        st.status == kStepSkipped ? 1 : st.result_k / h->interval + 1;
+    // Intervals the loop ran: one per check up to the deciding one, plus
+    // the unchecked first interval unless the step's first launch (with
+    // the reset and the ring part of bmax) ran ahead of the loop.
+    const long long checks = st.status == kStepSkipped
+                                 ? 1
+                                 : st.result_k / h->interval + (rhs_first ? 0 : 1);
     const long long iters = (checks + per_body - 1) / per_body;
-    return 2 + iters * (per_body * h->launches_per_check + 1);
+    return (rhs_first ? 3 : 2) + iters * (per_body * h->launches_per_check + 1);
 }
 
 // Outcome of a device-side step from its final state: sweeps or a status.
@@ -1021,9 +1059,12 @@ static long long run_device(jacobi_handle_t *h, const float *g, int steps,
     long long total = 0;
     for (int s = 0; s < steps; ++s) {
         const LoopState st = h->run_states_host[s];
-        // right-hand side (two copies for the first unfused step)
-        h->launches += (h->cfg.rhs == JACOBI_RHS_UNFUSED && s == 0) ? 2 : 1;
-        h->launches += device_step_launches(h, st) + (settle_needed ? 1 : 0);
+        // right-hand side (two copies for the first unfused step; none when
+        // the step's first sweep launch forms it)
+        if (!h->run_rhs_first)
+            h->launches += (h->cfg.rhs == JACOBI_RHS_UNFUSED && s == 0) ? 2 : 1;
+        h->launches += device_step_launches(h, st, h->run_rhs_first) +
+                       (settle_needed ? 1 : 0);
         const long long k = device_step_outcome(h, st);
         if (sweeps_per_step) sweeps_per_step[s] = k;
         if (k < 0) {

@@ -390,6 +390,11 @@ struct LaunchCtl {
     const int *stop;
     bool fused;
     LoopParams lp;
+    // First launch of a time step that forms the right-hand side itself
+    // (column-streamed kernel only): g and the b it writes; null otherwise.
+    // Its max |b| goes to lp.state->bmax.
+    const float *rhs_g;
+    float *rhs_b;
 };
 
 __device__ __forceinline__ unsigned warp_max_u(unsigned v) {
@@ -470,6 +475,24 @@ __device__ __forceinline__ void fused_block_finish(unsigned rm,
     loop_decide(lp, __fmul_rn(lp.d, __uint_as_float(bits)), st->bmax);
 }
 
+// Block-level max of the orderable bit patterns `v` (one per thread) into
+// *dst, one atomicMax per block. `scratch` is __shared__ space for 32
+// words. Every thread of the block must call it.
+__device__ __forceinline__ void block_max_into(unsigned v, unsigned *dst,
+                                               unsigned *scratch) {
+    const int tid = threadIdx.x + threadIdx.y * blockDim.x;
+    const int nthreads = blockDim.x * blockDim.y;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = (nthreads + 31) >> 5;
+    v = warp_max_u(v);
+    __syncthreads();  // scratch may alias memory the block used before
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    if (tid != 0) return;
+    unsigned bv = 0u;
+    for (int w = 0; w < nwarps; ++w) bv = max(bv, scratch[w]);
+    if (bv) atomicMax(dst, bv);
+}
+
 // |J(u) - u| of one cell as an orderable bit pattern (NaN above +Inf).
 __device__ __forceinline__ unsigned change_bits(float nv, float c) {
     return abs_bits(__fsub_rn(nv, c));
@@ -531,8 +554,10 @@ int sweep_sync_blocks(const GridDesc &g);
 // Status of a step that a multi-step graph skipped because an earlier step
 // failed (never returned to callers).
 constexpr int kStepSkipped = -100;
+// Fresh state for a step; k0: sweeps done before its first loop launch (one
+// check interval when the step's first launch runs ahead of the loop).
 cudaError_t launch_loop_reset(LoopState *st, const LoopState *prev,
-                              cudaStream_t stream);
+                              cudaStream_t stream, long long k0 = 0);
 // If st->where == 1, copy the interior of src (u_alt) into dst (u).
 cudaError_t launch_settle(const GridDesc &g, const LoopState *st,
                           const float *src, float *dst, cudaStream_t stream);
@@ -549,6 +574,12 @@ cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
 // bmax of the step's right-hand side into st->bmax (which must be 0).
 cudaError_t launch_bnorm(const GridDesc &g, const float *u, const float *b,
                          LoopState *st, cudaStream_t stream);
+// The part of bmax over the interior cells that have a Dirichlet-ring
+// neighbour, with b = fl(u + g) formed on the fly (for a step whose first
+// sweep launch forms b and reduces the other cells), folded into st->bmax.
+cudaError_t launch_bnorm_ring(const GridDesc &g, const float *u,
+                              const float *src, LoopState *st,
+                              cudaStream_t stream);
 
 // Tiled strategies (TMA-staged). Box = tile plus halo, read through the
 // tensor maps of the source field and of b.

@@ -88,13 +88,23 @@ __device__ __forceinline__ void cp_wait() {
 
 // One run of output rows [ya, yb) of the strip whose box starts at column
 // bxo. sw: this warp's staging slice (kSliceFloats floats).
-template <int D, bool FAST, bool EDGE, bool FUSED>
+//
+// FUSED: rmf accumulates max |J(u) - u| of the run's cells (level 1).
+// RHS (the first launch of a time step): bsrc is the source term g and the
+// launch forms the step's right-hand side b = fl(u + g) itself, from its
+// input u = u^n, as each row is staged: the levels read it from the b ring
+// as usual, the run's output cells of b go to bout, and rmf accumulates
+// max |b| over those of them that have no Dirichlet-ring neighbour (for
+// them b_I = b; the ring-adjacent cells are reduced by k_bnorm_ring).
+template <int D, bool FAST, bool EDGE, bool FUSED, bool RHS>
 __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
                                          const float *__restrict__ bsrc,
-                                         float *__restrict__ out, float *sw,
+                                         float *__restrict__ out,
+                                         float *__restrict__ bout, float *sw,
                                          int n, long long ld, float r, float d,
                                          float y, int bxo, int ya, int yb,
                                          float &rmf) {
+    static_assert(!(FUSED && RHS), "a right-hand-side launch checks nothing");
     using S = EtbsShape<D>;
     const int lane = threadIdx.x & 31;
     const int c0 = bxo + 4 * lane;  // this lane's first grid column
@@ -125,6 +135,14 @@ __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
     const float *pu = src + (long long)ra * ld + c0;
     const float *pb = bsrc + (long long)ra * ld + c0;
     float *po = out + (long long)(ra - D) * ld + c0;  // output row ra + t - D
+    float *pbo = RHS ? bout + (long long)ra * ld + c0 : nullptr;  // b, row ra + t
+    unsigned deepmask = 0xfu;  // cells of the lane with no ring neighbour
+    if (RHS && EDGE) {
+        deepmask = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            deepmask |= (c0 + k >= 2 && c0 + k <= n - 3) ? (1u << k) : 0u;
+    }
 
     auto issue = [&](int t) {  // stage input row ra + t (== row)
         // Interior runs stage rows and columns that all exist (the caller
@@ -163,6 +181,40 @@ __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
         issue(t + kAhead);
         cp_wait<kAhead>();  // row ra + t has landed
         float4 fresh = lds4(uown + (t & (kURing - 1)) * 128);  // level 0
+        if (RHS) {
+            // b of input row ra + t over its g, in both of its slots, before
+            // level 1 reads it at the next step.
+            float *bs = bown + (t & (kRing - 1)) * 128;
+            const float4 gq = lds4(bs);
+            const float4 bq = make_float4(
+                __fadd_rn(fresh.x, gq.x), __fadd_rn(fresh.y, gq.y),
+                __fadd_rn(fresh.z, gq.z), __fadd_rn(fresh.w, gq.w));
+            sts4(bs, bq);
+            sts4(bs + kRing * 128, bq);
+            const int i = ra + t;
+            if (in_tile && i >= ya && i < yb && colmask) {
+                if (colmask == 0xfu) {
+                    gst4(pbo, bq);
+                } else {
+                    if (colmask & 1u) gst1(pbo + 0, bq.x);
+                    if (colmask & 2u) gst1(pbo + 1, bq.y);
+                    if (colmask & 4u) gst1(pbo + 2, bq.z);
+                    if (colmask & 8u) gst1(pbo + 3, bq.w);
+                }
+                if (!EDGE) {
+                    rmf = max_nan_abs(rmf, bq.x);
+                    rmf = max_nan_abs(rmf, bq.y);
+                    rmf = max_nan_abs(rmf, bq.z);
+                    rmf = max_nan_abs(rmf, bq.w);
+                } else if (i >= 2 && i <= n - 3) {
+                    if (deepmask & 1u) rmf = max_nan_abs(rmf, bq.x);
+                    if (deepmask & 2u) rmf = max_nan_abs(rmf, bq.y);
+                    if (deepmask & 4u) rmf = max_nan_abs(rmf, bq.z);
+                    if (deepmask & 8u) rmf = max_nan_abs(rmf, bq.w);
+                }
+            }
+            pbo += ld;
+        }
         // b of row ra + t - k sits k - 1 slots below bk1 (level 1's)
         const float *bk1 = bown + (((t - 1) & (kRing - 1)) + kRing) * 128;
         const bool out_row = t >= 2 * D;
@@ -207,16 +259,18 @@ __device__ __forceinline__ void etbs_run(const float *__restrict__ src,
     cp_wait<0>();  // the rows staged past the run, before the slots are reused
 }
 
-template <int D, bool FAST, bool FUSED>
+// RHS: bsrc is g; the launch also writes the step's b into bout and folds
+// max |b| of the cells without ring neighbours into lp.state->bmax.
+template <int D, bool FAST, bool FUSED, bool RHS>
 __global__ void __launch_bounds__(32 * kWarps, 3)
 k_etbs(const float *__restrict__ src, const float *__restrict__ bsrc,
-       float *__restrict__ out, int n, long long ld, float r, float d, float y,
-       int strips, int *work, int bands, unsigned *err, const int *stop,
-       LoopParams lp) {
+       float *__restrict__ out, float *__restrict__ bout, int n, long long ld,
+       float r, float d, float y, int strips, int *work, int bands,
+       unsigned *err, const int *stop, LoopParams lp) {
     using S = EtbsShape<D>;
     __shared__ unsigned fin_scratch[33];
     extern __shared__ __align__(16) float smem[];  // kWarps slices
-    bounds_begin(smem, 0, out, nullptr, src, bsrc, n, ld, err);
+    bounds_begin(smem, 0, out, RHS ? bout : nullptr, src, bsrc, n, ld, err);
     allow_dependents();
     grid_dependency_wait();
     if (stop && *stop) return;  // same value for every thread of the launch
@@ -239,11 +293,11 @@ k_etbs(const float *__restrict__ src, const float *__restrict__ bsrc,
         const bool edge = bxo < 1 || bxo + 128 > n - 1 || ya - D < 1 ||
                           yb + D + kAhead > n;
         if (edge)
-            etbs_run<D, FAST, true, FUSED>(src, bsrc, out, sw, n, ld, r, d, y,
-                                           bxo, ya, yb, rmf);
+            etbs_run<D, FAST, true, FUSED, RHS>(src, bsrc, out, bout, sw, n, ld,
+                                                r, d, y, bxo, ya, yb, rmf);
         else
-            etbs_run<D, FAST, false, FUSED>(src, bsrc, out, sw, n, ld, r, d,
-                                            y, bxo, ya, yb, rmf);
+            etbs_run<D, FAST, false, FUSED, RHS>(src, bsrc, out, bout, sw, n,
+                                                 ld, r, d, y, bxo, ya, yb, rmf);
     }
     // The last warp out re-arms the work list for the next launch (a launch
     // starts only after the previous one has finished, PDL included).
@@ -257,6 +311,9 @@ k_etbs(const float *__restrict__ src, const float *__restrict__ bsrc,
         }
     }
     if (FUSED) fused_block_finish(__float_as_uint(rmf), lp, fin_scratch);
+    if (RHS) block_max_into(__float_as_uint(rmf),
+                            reinterpret_cast<unsigned *>(&lp.state->bmax),
+                            fin_scratch);
 }
 
 constexpr size_t kSmemBytes = (size_t)kWarps * kSliceFloats * sizeof(float);
@@ -269,7 +326,7 @@ cudaError_t prepare_d(TileConf &tc, int n) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, k_etbs<D, true, true>, 32 * kWarps, kSmemBytes);
+            &per_sm, k_etbs<D, true, true, false>, 32 * kWarps, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     // As many blocks as run at once; no more warps than strip rows.
@@ -288,12 +345,20 @@ cudaError_t launch_d(const GridDesc &g, const TileConf &tc, const float *src,
                      const LaunchCtl &ctl, cudaStream_t stream) {
     if (!tc.work || tc.bands < 1) return cudaErrorInvalidValue;
     const int strips = (g.n - 1 + EtbsShape<D>::TX - 1) / EtbsShape<D>::TX;
-#define TBJ_K(F, FU)                                                          \
-    launch_pdl(k_etbs<D, F, FU>, dim3(tc.ctas), dim3(32 * kWarps), kSmemBytes, \
-               stream, src, b, out, g.n, g.ld, g.r, g.d, g.y, strips,         \
+    const bool rhs = ctl.rhs_g != nullptr;
+    if (rhs && (ctl.fused || !ctl.rhs_b || !ctl.lp.state))
+        return cudaErrorInvalidValue;
+#define TBJ_K(F, FU, RH)                                                       \
+    launch_pdl(k_etbs<D, F, FU, RH>, dim3(tc.ctas), dim3(32 * kWarps),         \
+               kSmemBytes, stream, src, RH ? ctl.rhs_g : b, out,               \
+               RH ? ctl.rhs_b : nullptr, g.n, g.ld, g.r, g.d, g.y, strips,     \
                tc.work, tc.bands, err, ctl.stop, ctl.lp)
-    if (g.fast) return ctl.fused ? TBJ_K(true, true) : TBJ_K(true, false);
-    return ctl.fused ? TBJ_K(false, true) : TBJ_K(false, false);
+    if (g.fast) {
+        if (rhs) return TBJ_K(true, false, true);
+        return ctl.fused ? TBJ_K(true, true, false) : TBJ_K(true, false, false);
+    }
+    if (rhs) return TBJ_K(false, false, true);
+    return ctl.fused ? TBJ_K(false, true, false) : TBJ_K(false, false, false);
 #undef TBJ_K
 }
 
@@ -354,10 +419,12 @@ bool etbs_preferred(int n, int sms) {
 
 cudaError_t prepare_sweep_etbs(TileConf &tc, int n) {
     if (tc.depth != 8) return cudaErrorInvalidValue;
-    const void *kernels[4] = {(const void *)k_etbs<8, true, false>,
-                              (const void *)k_etbs<8, false, false>,
-                              (const void *)k_etbs<8, true, true>,
-                              (const void *)k_etbs<8, false, true>};
+    const void *kernels[6] = {(const void *)k_etbs<8, true, false, false>,
+                              (const void *)k_etbs<8, false, false, false>,
+                              (const void *)k_etbs<8, true, true, false>,
+                              (const void *)k_etbs<8, false, true, false>,
+                              (const void *)k_etbs<8, true, false, true>,
+                              (const void *)k_etbs<8, false, false, true>};
     for (const void *k : kernels) {
         cudaError_t e = cudaFuncSetAttribute(
             k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

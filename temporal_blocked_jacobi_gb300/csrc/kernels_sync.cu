@@ -286,6 +286,41 @@ k_bnorm(const float *__restrict__ u, const float *__restrict__ b,
 }
 
 // ---------------------------------------------------------------------------
+// The ring-adjacent part of bmax (rows 1 and n-2, columns 1 and n-2 of the
+// interior), for a step whose first sweep launch forms b = u + g and reduces
+// |b| over the other interior cells. Per cell the same b_I as k_bnorm, with
+// b = fl(u + g) formed here from u^n and the source g. Cells at a corner of
+// the interior are visited twice, which a maximum does not mind.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+k_bnorm_ring(const float *__restrict__ u, const float *__restrict__ g, int n,
+             long long ld, float r, LoopState *st) {
+    const int m = n - 2;  // interior cells per side
+    unsigned bm = 0u;
+    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < 4 * m;
+         idx += gridDim.x * blockDim.x) {
+        const int side = idx / m, pos = 1 + idx % m;
+        const int i = side == 0 ? 1 : side == 1 ? n - 2 : pos;
+        const int x = side == 2 ? 1 : side == 3 ? n - 2 : pos;
+        const long long p = (long long)i * ld + x;
+        const float bb = __fadd_rn(u[p], g[p]);
+        const float qw = (x == 1) ? u[p - 1] : 0.f;
+        const float qe = (x == n - 2) ? u[p + 1] : 0.f;
+        const float qn = (i == 1) ? u[p - ld] : 0.f;
+        const float qs = (i == n - 2) ? u[p + ld] : 0.f;
+        const float q = __fadd_rn(__fadd_rn(qw, qe), __fadd_rn(qn, qs));
+        bm = max(bm, abs_bits(__fadd_rn(bb, __fmul_rn(r, q))));
+    }
+    bm = warp_max(bm);
+    __shared__ unsigned s_b[8];
+    if ((threadIdx.x & 31) == 0) s_b[threadIdx.x >> 5] = bm;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) bm = max(bm, s_b[w]);
+    if (bm) atomicMax(reinterpret_cast<unsigned *>(&st->bmax), bm);
+}
+
+// ---------------------------------------------------------------------------
 // Fused right-hand side b = u + g and the interior copy dst = src: one float4
 // per thread, grid-stride over rows.
 // ---------------------------------------------------------------------------
@@ -363,12 +398,13 @@ __global__ void k_bounds_selftest(float *grid, int n, long long ld,
 // previous step's state: if that step did not converge, this step is marked
 // skipped (stopped before it starts), so every later kernel of it returns at
 // entry.
-__global__ void k_loop_reset(LoopState *st, const LoopState *prev) {
+__global__ void k_loop_reset(LoopState *st, const LoopState *prev,
+                             long long k0) {
     st->rmax = 0.f;
     st->bmax = 0.f;
     st->err = 0u;
     st->ticket = 0u;
-    st->k = 0;
+    st->k = k0;
     st->result_k = 0;
     st->stop = 0;
     st->status = 0;
@@ -483,8 +519,8 @@ int sweep_sync_blocks(const GridDesc &g) {
 }
 
 cudaError_t launch_loop_reset(LoopState *st, const LoopState *prev,
-                              cudaStream_t stream) {
-    k_loop_reset<<<1, 1, 0, stream>>>(st, prev);
+                              cudaStream_t stream, long long k0) {
+    k_loop_reset<<<1, 1, 0, stream>>>(st, prev, k0);
     return cudaGetLastError();
 }
 
@@ -527,6 +563,15 @@ cudaError_t launch_residual(const GridDesc &g, const float *u, const float *b,
     }
 #undef TBJ_RESID
 #undef TBJ_RESID_K
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bnorm_ring(const GridDesc &g, const float *u,
+                              const float *src, LoopState *st,
+                              cudaStream_t stream) {
+    const long long cells = 4LL * (g.n - 2);
+    const int blocks = (int)((cells + 255) / 256 < 152 ? (cells + 255) / 256 : 152);
+    k_bnorm_ring<<<blocks, 256, 0, stream>>>(u, src, g.n, g.ld, g.r, st);
     return cudaGetLastError();
 }
 
