@@ -287,6 +287,10 @@ int jacobi_set_strategy(jacobi_handle_t *h, const jacobi_config_t *cfg);
  * `steps` steps, jacobi_rhs(g) then jacobi_solve_step; u^{n+1} replaces u^n
  * in u. sweeps_per_step (host, `steps` entries, may be NULL) receives each
  * step's count. Returns the total sweep count or the first negative status.
+ * b holds the last step's right-hand side afterwards. Under device control
+ * with the column-streamed ETB(8) kernel and one launch per check interval,
+ * each step's first sweep launch forms b = u^n + g itself (section 05 on
+ * fusing the right-hand side); the results are the same bits.
  */
 long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
                      long long *sweeps_per_step);
