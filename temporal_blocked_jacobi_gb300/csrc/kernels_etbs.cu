@@ -408,13 +408,16 @@ int etbs_schedule(const TileConf &tc, int n, int *band_start, int cap) {
 }
 
 bool etbs_preferred(int n, int sms) {
-    // Rows per warp of the whole launch at 12 warps per SM: below about two
-    // hundred the pipeline's fill and drain (2 D rows per run) and the
-    // launch's last runs outweigh the saved halo (measured on GB300 at D = 8:
-    // N = 4096 is faster with the register-band kernel, N = 8192 with this
-    // one).
+    // Rows per warp of the whole launch at 12 warps per SM: below about 64
+    // the pipeline's fill and drain (2 D rows per run) and the launch's last
+    // runs outweigh the saved halo. Measured on GB300, ten-step solves at
+    // D = 8 under device control (this kernel also forms each step's
+    // right-hand side there), register-band kernel against this one:
+    // N = 3072 (47 rows per warp) 28.0 against 32.8 ms; N = 4096 (83)
+    // 42.6 against 40.5 ms at r = 10, 6.71 against 6.04 at r = 1, 310.1
+    // against 297.6 at r = 100; N = 6144 88.5 against 80.3.
     const long long strips = (n - 1 + EtbsShape<8>::TX - 1) / EtbsShape<8>::TX;
-    return (long long)(n - 2) * strips >= 192LL * 12 * sms;
+    return (long long)(n - 2) * strips >= 64LL * 12 * sms;
 }
 
 cudaError_t prepare_sweep_etbs(TileConf &tc, int n) {
