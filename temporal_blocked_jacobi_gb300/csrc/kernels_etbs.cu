@@ -30,10 +30,12 @@
 // most kBandMax and at least kBandMin rows), so the launch ends with short
 // runs instead of a long tail. The last warp to finish resets the counter
 // for the next launch. Measured on GB300 at N = 8192 / 12288 / 18432 (us
-// per launch): these settings 236 / 477 / 959; runs of the work left over
-// the warps alone, 64 to 256 rows, 247 / 461 / 978; fixed 128-row runs
-// 229 / 474 / 1028; fixed 256 235 / - / 983; one static share per warp
-// 272 / - / 1294.
+// per launch, when these settings took 236 / 477 / 959): runs of the work
+// left over the warps alone, 64 to 256 rows, 247 / 461 / 978; fixed
+// 128-row runs 229 / 474 / 1028; fixed 256 235 / - / 983; one static share
+// per warp 272 / - / 1294. With the current source (230 / - / 924 us), a
+// largest run of 256, 384, 640, 1024 or 2048 rows instead of 512 takes
+// 933, 934, 949, 1002, 1002 us at N = 18432.
 //
 // Input rows reach the warp through rings of rows of u and b in its slice
 // of shared memory, filled with cp.async kAhead rows ahead; a row's b stays
@@ -41,6 +43,11 @@
 // Lane l copies and reads back only its own 16 bytes of each row. Rows and
 // columns outside the array are zero-filled. Cells that are not interior
 // grid cells keep their value at every level (the Dirichlet ring).
+//
+// Three variants: plain; residual-fused (the device-side loop's launches:
+// level 1 also reduces max |J(u) - u| of the launch's input); and
+// right-hand-side (a time step's first launch in a whole run: it forms
+// b = u^n + g as the rows of u^n arrive).
 //
 // Compiled for D = 8, the depth it is made for: at D = 4 the register-band
 // kernel is already close to the HBM bound, and at D = 16 the 2*D rows of

@@ -228,7 +228,31 @@ def test_n4096_gauss(r):
         {"strategy": "sync", "depth": 1, "control": "device"},
         {"strategy": "etb", "depth": 4, "control": "device"},
         {"strategy": "etb", "depth": 8, "control": "device"},
+        {"strategy": "etb", "depth": 8, "tile": (112, 92), "control": "device"},
         {"strategy": "sync", "depth": 1, "rhs": "unfused", "control": "device"}])
+
+
+@pytest.mark.parametrize("n", [3530, 3585, 3586, 4097])
+def test_etb8_default_around_the_streamed_threshold(n):
+    """Sizes on both sides of where the D = 8 default turns from the
+    register-band to the column-streamed kernel (64 rows per warp): two time
+    steps of the default ETB(8) under device control equal SYNC's, sweep
+    counts and fields bit for bit (SYNC being pinned to the oracle)."""
+    import torch
+    from temporal_blocked_jacobi_gb300 import jacobi
+    u0, g = workload(n, "gauss")
+    ref_u, ref_k, _ = gpu_run(u0, g, 10.0, steps=2, control="device")
+    got_u, got_k, _ = gpu_run(u0, g, 10.0, steps=2, strategy="etb", depth=8,
+                              control="device")
+    assert got_k == ref_k
+    assert same_bits(got_u, ref_u), mismatch(got_u, ref_u)
+    u, u_alt, b = jacobi.allocate(n, u0.shape[1])
+    with jacobi.Solver(u, u_alt, b, 10.0, strategy="etb", depth=8) as s:
+        streamed = s.tile == (112, 0)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    strips = -(-(n - 1) // 112)
+    assert streamed == ((n - 2) * strips >= 64 * 12 * sms)
 
 
 def test_n8192_r100_gauss():
