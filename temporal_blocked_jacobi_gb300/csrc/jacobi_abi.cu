@@ -66,7 +66,8 @@ struct jacobi_handle {
     LoopState *run_states_host = nullptr;  // pinned copy
     int run_cap = 0;
     // The run graph's steps start with a sweep launch that forms b itself
-    // (rhs_first_launch) instead of k_rhs and k_bnorm.
+    // (rhs_first_launch) instead of k_rhs and k_bnorm, each from the buffer
+    // that holds the previous step's answer (record_run_rhs_first).
     bool run_rhs_first = false;
     int cur = 0;  // 0: the iterate is in u; 1: in u_alt
 
@@ -548,6 +549,143 @@ bool rhs_first_launch(const jacobi_handle_t *h) {
            h->tc.variant == kEtbsVariant && h->launches_per_check == 1;
 }
 
+// Capture what `fn` enqueues on the capture stream into graph `gr`, after
+// node `dep` (null: none); *last receives the one node it ends in.
+template <class F>
+cudaError_t capture_into(jacobi_handle_t *h, cudaGraph_t gr, cudaGraphNode_t dep,
+                         F fn, cudaGraphNode_t *last) {
+    cudaError_t e = cudaStreamBeginCaptureToGraph(
+        h->capture, gr, dep ? &dep : nullptr, nullptr, dep ? 1 : 0,
+        cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return e;
+    e = fn();
+    if (e == cudaSuccess && last) {
+        cudaStreamCaptureStatus cs;
+        const cudaGraphNode_t *deps = nullptr;
+        size_t ndeps = 0;
+        e = cudaStreamGetCaptureInfo(h->capture, &cs, nullptr, nullptr, &deps,
+                                     nullptr, &ndeps);
+        if (e == cudaSuccess) {
+            if (ndeps == 1) *last = deps[0];
+            else e = cudaErrorStreamCaptureUnmatched;
+        }
+    }
+    cudaGraph_t g2 = nullptr;
+    cudaError_t e2 = cudaStreamEndCapture(h->capture, &g2);
+    return e != cudaSuccess ? e : e2;
+}
+
+// One way through a step of a run that starts each step with the launch
+// that forms b (rhs_first_launch), into graph `gr` after `dep`, for u^n in
+// buffer `sb` (0: u, 1: u_alt): bmax of the ring-adjacent cells -> the first
+// launch, sb -> the other buffer -> WHILE(cond) { loop body from there }.
+cudaError_t add_rhs_first_step(jacobi_handle_t *h, cudaGraph_t gr,
+                               cudaGraphNode_t dep, LoopState *st,
+                               const float *g, int sb,
+                               cudaGraphNode_t *loop_out) {
+    cudaGraphConditionalHandle cond{};
+    cudaError_t e = cudaGraphConditionalHandleCreate(&cond, gr, 1,
+                                                     cudaGraphCondAssignDefault);
+    cudaGraphNode_t head = nullptr;
+    if (e == cudaSuccess)
+        e = capture_into(h, gr, dep, [&]() {
+            cudaError_t r = launch_bnorm_ring(h->g, sb ? h->u_alt : h->u, g, st,
+                                              h->capture);
+            if (r != cudaSuccess) return r;
+            LaunchCtl c = loop_ctl(h, st, false, sb, cond);
+            c.rhs_g = g;
+            c.rhs_b = h->b;
+            return enqueue_launch(h, sb, h->capture, c);
+        }, &head);
+    cudaGraph_t body = nullptr;
+    if (e == cudaSuccess) {
+        cudaGraphNodeParams p = {};
+        p.type = cudaGraphNodeTypeConditional;
+        p.conditional.handle = cond;
+        p.conditional.type = cudaGraphCondTypeWhile;
+        p.conditional.size = 1;
+        cudaGraphNode_t loop_node = nullptr;
+        e = cudaGraphAddNode(&loop_node, gr, &head, nullptr, 1, &p);
+        if (e == cudaSuccess) body = p.conditional.phGraph_out[0];
+        if (loop_out) *loop_out = loop_node;
+    }
+    if (e == cudaSuccess)
+        e = capture_into(h, body, nullptr,
+                         [&]() { return capture_body(h, st, cond, 1 - sb); }, nullptr);
+    return e;
+}
+
+// Device control, whole run, each step starting with the launch that forms
+// b. A step's answer stays in whichever buffer holds it, and the next step
+// starts from there: step s > 0 is an if/else node on the previous step's
+// LoopState::where whose two branches are add_rhs_first_step from u and
+// from u_alt (step 0 starts from u). Only the run's answer is moved into u,
+// at the end:
+//   [reset(s) -> choose branch -> IF { from u } ELSE { from u_alt }] x steps
+//   -> settle (u_alt -> u when the last answer is there) -> states to host
+int record_run_rhs_first(jacobi_handle_t *h, const float *g, int steps) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaGraphCreate(&graph, 0);
+    cudaGraphNode_t prev = nullptr;
+    for (int s = 0; s < steps && e == cudaSuccess; ++s) {
+        LoopState *st = h->run_states + s;
+        LoopState *pst = s ? st - 1 : nullptr;
+        cudaGraphConditionalHandle ifc{};
+        if (s > 0)
+            e = cudaGraphConditionalHandleCreate(&ifc, graph, 0,
+                                                 cudaGraphCondAssignDefault);
+        cudaGraphNode_t head = nullptr;
+        if (e == cudaSuccess)
+            e = capture_into(h, graph, prev, [&]() {
+                cudaError_t r = launch_loop_reset(st, pst, h->capture,
+                                                  h->interval, true);
+                if (r == cudaSuccess && s > 0)
+                    r = launch_branch_on_where(pst, ifc, h->capture);
+                return r;
+            }, &head);
+        if (e != cudaSuccess) break;
+        if (s == 0) {
+            e = add_rhs_first_step(h, graph, head, st, g, 0, &prev);
+        } else {
+            cudaGraphNodeParams p = {};
+            p.type = cudaGraphNodeTypeConditional;
+            p.conditional.handle = ifc;
+            p.conditional.type = cudaGraphCondTypeIf;
+            p.conditional.size = 2;
+            cudaGraphNode_t if_node = nullptr;
+            e = cudaGraphAddNode(&if_node, graph, &head, nullptr, 1, &p);
+            if (e == cudaSuccess)
+                e = add_rhs_first_step(h, p.conditional.phGraph_out[0], nullptr,
+                                       st, g, 0, nullptr);
+            if (e == cudaSuccess)
+                e = add_rhs_first_step(h, p.conditional.phGraph_out[1], nullptr,
+                                       st, g, 1, nullptr);
+            prev = if_node;
+        }
+    }
+    LoopState *last_st = h->run_states + (steps - 1);
+    if (e == cudaSuccess)
+        e = capture_into(h, graph, prev, [&]() {
+            cudaError_t r = launch_settle(h->g, last_st, h->u_alt, h->u, h->capture);
+            if (r == cudaSuccess)
+                r = cudaMemcpyAsync(h->run_states_host, h->run_states,
+                                    sizeof(LoopState) * steps,
+                                    cudaMemcpyDeviceToHost, h->capture);
+            return r;
+        }, nullptr);
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&h->run, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, JACOBI_ERR_CUDA, "recording the run graph: %s",
+                    cudaGetErrorString(e));
+    }
+    h->run_rhs_first = true;
+    h->run_g = g;
+    h->run_steps = steps;
+    return JACOBI_OK;
+}
+
 int record_run(jacobi_handle_t *h, const float *g, int steps) {
     h->run_rhs_first = false;
     if (h->cfg.control == JACOBI_CONTROL_PERSISTENT)
@@ -566,8 +704,8 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
         TBJ_CUDA(h, cudaMallocHost(&h->run_states_host, sizeof(LoopState) * steps));
         h->run_cap = steps;
     }
+    if (rhs_first_launch(h)) return record_run_rhs_first(h, g, steps);
     const bool settle_needed = h->launches_per_check % 2 == 1;
-    const bool rhs_first = rhs_first_launch(h);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaGraphCreate(&graph, 0);
     auto check = [&](cudaError_t err) {
@@ -585,28 +723,14 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
             check(cudaStreamBeginCaptureToGraph(
                 h->capture, graph, prev ? &prev : nullptr, nullptr,
                 prev ? 1 : 0, cudaStreamCaptureModeThreadLocal))) {
-            if (rhs_first) {
-                // reset (the loop starts one interval in) -> bmax of the
-                // ring-adjacent cells -> the step's first launch, u -> u_alt,
-                // which forms b and the rest of bmax.
-                check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture,
-                                        h->interval));
-                check(launch_bnorm_ring(h->g, h->u, g, st, h->capture));
-                LaunchCtl c = loop_ctl(h, st, false, 0, cond);
-                c.rhs_g = g;
-                c.rhs_b = h->b;
-                check(enqueue_launch(h, 0, h->capture, c));
+            if (h->cfg.rhs == JACOBI_RHS_UNFUSED) {
+                if (s == 0) check(launch_copy_interior(h->g, g, h->g_copy, h->capture));
+                check(launch_copy_interior(h->g, h->u, h->b, h->capture));
             } else {
-                if (h->cfg.rhs == JACOBI_RHS_UNFUSED) {
-                    if (s == 0)
-                        check(launch_copy_interior(h->g, g, h->g_copy, h->capture));
-                    check(launch_copy_interior(h->g, h->u, h->b, h->capture));
-                } else {
-                    check(launch_rhs(h->g, h->u, g, h->b, h->capture));
-                }
-                check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture));
-                check(launch_bnorm(h->g, h->u, h->b, st, h->capture));
+                check(launch_rhs(h->g, h->u, g, h->b, h->capture));
             }
+            check(launch_loop_reset(st, s ? st - 1 : nullptr, h->capture));
+            check(launch_bnorm(h->g, h->u, h->b, st, h->capture));
             cudaStreamCaptureStatus cs;
             const cudaGraphNode_t *deps = nullptr;
             size_t ndeps = 0;
@@ -631,7 +755,7 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
         if (e == cudaSuccess &&
             check(cudaStreamBeginCaptureToGraph(h->capture, body, nullptr, nullptr,
                                                 0, cudaStreamCaptureModeThreadLocal))) {
-            check(capture_body(h, st, cond, rhs_first ? 1 : 0));
+            check(capture_body(h, st, cond));
             cudaGraph_t g2 = nullptr;
             check(cudaStreamEndCapture(h->capture, &g2));
         }
@@ -669,7 +793,6 @@ int record_run(jacobi_handle_t *h, const float *g, int steps) {
         return fail(h, JACOBI_ERR_CUDA, "recording the run graph: %s",
                     cudaGetErrorString(e));
     }
-    h->run_rhs_first = rhs_first;
     h->run_g = g;
     h->run_steps = steps;
     return JACOBI_OK;
@@ -1054,28 +1177,35 @@ static long long run_device(jacobi_handle_t *h, const float *g, int steps,
     TBJ_CUDA(h, cudaGraphLaunch(h->run, h->stream));
     TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
     h->b_mode = h->cfg.rhs;
-    const bool settle_needed = h->launches_per_check % 2 == 1 ||
-                               h->cfg.control == JACOBI_CONTROL_PERSISTENT;
+    const bool rf = h->run_rhs_first;
+    const bool settle_each = !rf && (h->launches_per_check % 2 == 1 ||
+                                     h->cfg.control == JACOBI_CONTROL_PERSISTENT);
+    // Kernels step s ran: its own (device_step_launches) plus, when steps
+    // start with the launch that forms b, the branch choice of steps > 0;
+    // otherwise the right-hand side (two copies for the first unfused step)
+    // and the per-step settle where intervals have an odd launch count.
+    auto step_launches = [&](int s, const LoopState &st) {
+        long long n = device_step_launches(h, st, rf);
+        if (rf) return n + (s > 0 ? 1 : 0);
+        return n + ((h->cfg.rhs == JACOBI_RHS_UNFUSED && s == 0) ? 2 : 1) +
+               (settle_each ? 1 : 0);
+    };
     long long total = 0;
     for (int s = 0; s < steps; ++s) {
         const LoopState st = h->run_states_host[s];
-        // right-hand side (two copies for the first unfused step; none when
-        // the step's first sweep launch forms it)
-        if (!h->run_rhs_first)
-            h->launches += (h->cfg.rhs == JACOBI_RHS_UNFUSED && s == 0) ? 2 : 1;
-        h->launches += device_step_launches(h, st, h->run_rhs_first) +
-                       (settle_needed ? 1 : 0);
+        h->launches += step_launches(s, st);
         const long long k = device_step_outcome(h, st);
         if (sweeps_per_step) sweeps_per_step[s] = k;
         if (k < 0) {
             // later steps were skipped on the device: count their kernels
             for (int q = s + 1; q < steps; ++q)
-                h->launches += 1 + device_step_launches(h, h->run_states_host[q]) +
-                               (settle_needed ? 1 : 0);
+                h->launches += step_launches(q, h->run_states_host[q]);
+            if (rf) h->launches += 1;  // the run's final settle
             return k;
         }
         total += k;
     }
+    if (rf) h->launches += 1;  // the run's final settle
     return total;
 }
 

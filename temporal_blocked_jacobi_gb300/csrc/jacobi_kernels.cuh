@@ -556,8 +556,16 @@ int sweep_sync_blocks(const GridDesc &g);
 constexpr int kStepSkipped = -100;
 // Fresh state for a step; k0: sweeps done before its first loop launch (one
 // check interval when the step's first launch runs ahead of the loop).
+// keep_where: a step skipped after a failure takes over the failed step's
+// LoopState::where (runs whose steps start from either buffer).
 cudaError_t launch_loop_reset(LoopState *st, const LoopState *prev,
-                              cudaStream_t stream, long long k0 = 0);
+                              cudaStream_t stream, long long k0 = 0,
+                              bool keep_where = false);
+// Set the if/else condition `cond` to 1 when the previous step's answer is
+// in u (LoopState::where == 0), else 0.
+cudaError_t launch_branch_on_where(const LoopState *prev,
+                                   cudaGraphConditionalHandle cond,
+                                   cudaStream_t stream);
 // If st->where == 1, copy the interior of src (u_alt) into dst (u).
 cudaError_t launch_settle(const GridDesc &g, const LoopState *st,
                           const float *src, float *dst, cudaStream_t stream);

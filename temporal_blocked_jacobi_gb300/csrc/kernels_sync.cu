@@ -399,7 +399,7 @@ __global__ void k_bounds_selftest(float *grid, int n, long long ld,
 // skipped (stopped before it starts), so every later kernel of it returns at
 // entry.
 __global__ void k_loop_reset(LoopState *st, const LoopState *prev,
-                             long long k0) {
+                             long long k0, int keep_where) {
     st->rmax = 0.f;
     st->bmax = 0.f;
     st->err = 0u;
@@ -415,7 +415,16 @@ __global__ void k_loop_reset(LoopState *st, const LoopState *prev,
     if (prev && prev->status != 0) {
         st->status = kStepSkipped;
         st->stop = 1;
+        // The run's answer stays where the failed step left it.
+        if (keep_where) st->where = prev->where;
     }
+}
+
+// Condition of a step's if/else node in a run whose steps start from
+// wherever the previous step's answer is: 1 (first branch) when it is in u.
+__global__ void k_branch_on_where(const LoopState *prev,
+                                  cudaGraphConditionalHandle cond) {
+    cudaGraphSetConditional(cond, prev->where == 0 ? 1u : 0u);
 }
 
 // End of a time step in a multi-step graph: if the answer sits in u_alt
@@ -519,8 +528,9 @@ int sweep_sync_blocks(const GridDesc &g) {
 }
 
 cudaError_t launch_loop_reset(LoopState *st, const LoopState *prev,
-                              cudaStream_t stream, long long k0) {
-    k_loop_reset<<<1, 1, 0, stream>>>(st, prev, k0);
+                              cudaStream_t stream, long long k0,
+                              bool keep_where) {
+    k_loop_reset<<<1, 1, 0, stream>>>(st, prev, k0, keep_where ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -528,6 +538,13 @@ cudaError_t launch_settle(const GridDesc &g, const LoopState *st,
                           const float *src, float *dst, cudaStream_t stream) {
     k_settle<<<elementwise_grid(g.n), dim3(32, 8), 0, stream>>>(st, src, dst,
                                                                 g.n, g.ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_branch_on_where(const LoopState *prev,
+                                  cudaGraphConditionalHandle cond,
+                                  cudaStream_t stream) {
+    k_branch_on_where<<<1, 1, 0, stream>>>(prev, cond);
     return cudaGetLastError();
 }
 

@@ -7,10 +7,12 @@ Under device control, with exact temporal blocking at D = 8 in whole columns
 (tile 112 x 0) and one launch per check interval, each step of jacobi_run is
 reset -> bmax of the ring-adjacent cells -> the first sweep launch, which
 forms b = fl(u^n + g) from the u^n it reads, writes it, and reduces |b| over
-the other cells -> the device-side loop from its output. The sweep counts,
-fields and the last step's b must equal the oracle's, bit for bit, whatever
-cell holds max |b_I|; errors and launch counts behave as on the ordinary
-path.
+the other cells -> the device-side loop from its output. A step starts from
+whichever buffer holds the previous step's answer (an if/else graph node),
+and only the run's answer is moved into u. The sweep counts, fields and the
+last step's b must equal the oracle's, bit for bit, whatever cell holds
+max |b_I| and whichever buffer each step ends in; errors and launch counts
+behave as on the ordinary path.
 """
 import ctypes
 
@@ -123,10 +125,12 @@ def test_sweep_cap_reports_not_converged():
 
 @pytest.mark.parametrize("n", [64, 1030])
 def test_launch_count(n):
-    """Per step: the reset, the ring part of bmax, the first launch, then
-    loop iterations of `body` launches and one loop-condition kernel until
-    the check that stops (the first launch covered the unchecked first
-    interval), then the kernel that moves the answer into u."""
+    """Per step: the reset, the branch choice (steps after the first: the
+    step starts from the buffer holding the previous answer), the ring part
+    of bmax, the first launch, then loop iterations of `body` launches and
+    one loop-condition kernel until the check that stops (the first launch
+    covered the unchecked first interval); at the end one kernel moves the
+    run's answer into u."""
     import torch
     from temporal_blocked_jacobi_gb300 import jacobi
     u0, g = workload(n, "point")
@@ -136,6 +140,7 @@ def test_launch_count(n):
         c0 = s.launch_count
         counts = s.run(to_dev(g), 3)
         body = 16 if n >= 1024 else 8
-        expected = sum(3 + -(-(k // 8) // body) * (body + 1) + 1 for k in counts)
+        expected = 1 + sum(3 + (s > 0) + -(-(k // 8) // body) * (body + 1)
+                           for s, k in enumerate(counts))
         assert s.launch_count - c0 == expected
     torch.cuda.synchronize()
