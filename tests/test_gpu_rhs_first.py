@@ -29,8 +29,9 @@ STREAMED = dict(strategy="etb", depth=8, tile=(112, 0), control="device")
 
 
 @pytest.mark.parametrize("n,r,source", [(3, 10.0, "point"), (17, 1.0, "point"),
-                                        (70, 10.0, "gauss"), (131, 1.0, "point"),
-                                        (300, 10.0, "gauss"), (1030, 1.0, "gauss")])
+                                        (70, 10.0, "gauss"), (70, 10.0, "zero"),
+                                        (131, 1.0, "point"), (300, 10.0, "gauss"),
+                                        (1030, 1.0, "gauss")])
 def test_first_launch_forms_the_right_hand_side(n, r, source):
     u0, g = workload(n, source)
     ref_u, ref_k, ref_b = oracle.run(u0, g, r, steps=3)
