@@ -624,6 +624,8 @@ cudaError_t add_rhs_first_step(jacobi_handle_t *h, cudaGraph_t gr,
 //   [reset(s) -> choose branch -> IF { from u } ELSE { from u_alt }] x steps
 //   -> settle (u_alt -> u when the last answer is there) -> states to host
 int record_run_rhs_first(jacobi_handle_t *h, const float *g, int steps) {
+    if (steps < 1)
+        return fail(h, JACOBI_ERR_INVALID_ARG, "a run graph needs steps >= 1");
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaGraphCreate(&graph, 0);
     cudaGraphNode_t prev = nullptr;
