@@ -307,13 +307,16 @@ long long jacobi_run(jacobi_handle_t *h, const float *g, int steps,
  *
  * The host-device copies overlap the solves: problem i + 1's inputs are
  * copied in, and problem i - 1's result out, while problem i is solved, on
- * a stream of the handle's own. Host buffers should be pinned
- * (cudaHostAlloc or equivalent) for the copies to be asynchronous. u, u_alt
- * are overwritten (u holds the last problem's result on return), and b
- * receives the right-hand sides. On first use the handle allocates four
- * device buffers of N*ld floats (staging for the copies), a stream and four
- * events, kept until jacobi_destroy. Synchronous: returns when every result
- * is in host memory.
+ * a stream of the handle's own. Problems alternate between the handle's
+ * fields and a second pair of fields solved by a twin handle (same
+ * configuration, b and stream), so inputs and results move straight
+ * between host memory and the fields that are solved. Host buffers should
+ * be pinned (cudaHostAlloc or equivalent) for the copies to be
+ * asynchronous. u, u_alt are overwritten (u holds the last problem's result
+ * on return), and b receives the right-hand sides. On first use the handle
+ * allocates four device buffers of N*ld floats (the twin's two fields and
+ * the two sources), the twin handle, a stream and two events, kept until
+ * jacobi_destroy. Synchronous: returns when every result is in host memory.
  */
 long long jacobi_run_host(jacobi_handle_t *h, int count,
                           const float *const *u0_host,

@@ -39,14 +39,16 @@ struct jacobi_handle {
     CUtensorMap map_u{}, map_alt{}, map_b{};
     int *etbs_work = nullptr;  // column-streamed ETB: its work list (device)
 
-    // Host-buffer runs (jacobi_run_host), allocated on first use: the next
-    // problem's u0 and g staged on the device, the g of the problem being
-    // solved, the last result on its way out, and a stream for the copies.
-    float *hb_u = nullptr, *hb_g = nullptr, *hb_gdev = nullptr, *hb_out = nullptr;
+    // Host-buffer runs (jacobi_run_host), allocated on first use: a twin
+    // handle over a second pair of fields (hb_tu, hb_tualt; it shares b and
+    // the stream), the source of each handle's problems (hb_g[0] for this
+    // handle, hb_g[1] for the twin), a stream for the copies and, per pair,
+    // an event marking its next problem's inputs in place.
+    jacobi_handle_t *hb_twin = nullptr;
+    float *hb_tu = nullptr, *hb_tualt = nullptr;
+    float *hb_g[2] = {nullptr, nullptr};
     cudaStream_t hb_copy = nullptr;
-    // inputs staged, inputs taken, result staged, result copied out
-    cudaEvent_t hb_staged = nullptr, hb_taken = nullptr, hb_result = nullptr,
-                hb_copied = nullptr;
+    cudaEvent_t hb_staged[2] = {nullptr, nullptr};
 
     // Sweeps per launch, launches per check, sweeps per check.
     int per_launch = 1;
@@ -1427,9 +1429,10 @@ void jacobi_destroy(jacobi_handle_t *h) {
     if (h->loop_host) cudaFreeHost(h->loop_host);
     if (h->g_copy) cudaFree(h->g_copy);
     if (h->hb_copy) cudaStreamSynchronize(h->hb_copy);
-    for (float *p : {h->hb_u, h->hb_g, h->hb_gdev, h->hb_out})
+    if (h->hb_twin) jacobi_destroy(h->hb_twin);
+    for (float *p : {h->hb_tu, h->hb_tualt, h->hb_g[0], h->hb_g[1]})
         if (p) cudaFree(p);
-    for (cudaEvent_t e : {h->hb_staged, h->hb_taken, h->hb_result, h->hb_copied})
+    for (cudaEvent_t e : h->hb_staged)
         if (e) cudaEventDestroy(e);
     if (h->hb_copy) cudaStreamDestroy(h->hb_copy);
     delete h;
@@ -1447,60 +1450,82 @@ long long jacobi_run_host(jacobi_handle_t *h, int count,
         if (!u0_host[i] || !g_host[i] || !u_host[i])
             return fail(h, JACOBI_ERR_INVALID_ARG, "problem %d has a NULL buffer", i);
     const size_t bytes = sizeof(float) * (size_t)h->g.n * (size_t)h->g.ld;
-    if (!h->hb_copy) {  // first use: device staging, copy stream, events
-        TBJ_CUDA(h, cudaMalloc(&h->hb_u, bytes));
-        TBJ_CUDA(h, cudaMalloc(&h->hb_g, bytes));
-        TBJ_CUDA(h, cudaMalloc(&h->hb_gdev, bytes));
-        TBJ_CUDA(h, cudaMalloc(&h->hb_out, bytes));
-        for (cudaEvent_t *e : {&h->hb_staged, &h->hb_taken, &h->hb_result, &h->hb_copied})
-            TBJ_CUDA(h, cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    if (!h->hb_copy) {  // first use: the twin's fields, the sources, copy stream, events
+        TBJ_CUDA(h, cudaMalloc(&h->hb_tu, bytes));
+        TBJ_CUDA(h, cudaMalloc(&h->hb_tualt, bytes));
+        TBJ_CUDA(h, cudaMalloc(&h->hb_g[0], bytes));
+        TBJ_CUDA(h, cudaMalloc(&h->hb_g[1], bytes));
+        TBJ_CUDA(h, cudaMemsetAsync(h->hb_tu, 0, bytes, h->stream));
+        for (cudaEvent_t &e : h->hb_staged)
+            TBJ_CUDA(h, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
         TBJ_CUDA(h, cudaStreamCreateWithFlags(&h->hb_copy, cudaStreamNonBlocking));
     }
+    // The twin solves the odd problems, on its own fields and with this
+    // handle's configuration, b and stream.
+    if (!h->hb_twin) {
+        int rc = jacobi_create(&h->hb_twin, h->g.n, h->g.ld, h->g.r, &h->cfg,
+                               h->hb_tu, h->hb_tualt, h->b, h->stream);
+        if (rc) {
+            h->hb_twin = nullptr;
+            return fail(h, rc, "creating the second solver of jacobi_run_host: %s",
+                        jacobi_last_error(nullptr));
+        }
+    } else if (std::memcmp(&h->hb_twin->cfg, &h->cfg, sizeof h->cfg) != 0) {
+        if (int rc = jacobi_set_strategy(h->hb_twin, &h->cfg))
+            return fail(h, rc, "%s", jacobi_last_error(h->hb_twin));
+    }
+    jacobi_handle_t *hs[2] = {h, h->hb_twin};
     cudaStream_t cs = h->hb_copy;
-    // The copy stream starts after everything already queued on the handle's
-    // stream (the caller may have been using the buffers).
-    TBJ_CUDA(h, cudaEventRecord(h->hb_result, h->stream));
-    TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_result, 0));
-    TBJ_CUDA(h, cudaEventRecord(h->hb_copied, cs));
-    TBJ_CUDA(h, cudaMemcpyAsync(h->hb_u, u0_host[0], bytes, cudaMemcpyHostToDevice, cs));
-    TBJ_CUDA(h, cudaMemcpyAsync(h->hb_g, g_host[0], bytes, cudaMemcpyHostToDevice, cs));
-    TBJ_CUDA(h, cudaEventRecord(h->hb_staged, cs));
+    int rc = settle(h);  // this handle's iterate back in u before its buffers are reused
+    if (rc) return rc;
+    // Problem i runs on hs[i % 2]. Its inputs go straight into that
+    // handle's u (and the Dirichlet ring into its u_alt) and into
+    // hb_g[i % 2], on the copy stream, while problem i - 1 runs; its result
+    // leaves from that u while problem i + 1 runs. The copy stream takes
+    // things in order, so a pair's next inputs come in only after its last
+    // result has gone out.
+    TBJ_CUDA(h, cudaEventRecord(h->hb_staged[0], h->stream));
+    TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_staged[0], 0));
+    auto stage = [&](int i) -> int {
+        jacobi_handle_t *t = hs[i % 2];
+        TBJ_CUDA(h, cudaMemcpyAsync(t->u, u0_host[i], bytes, cudaMemcpyHostToDevice, cs));
+        TBJ_CUDA(h, cudaMemcpyAsync(h->hb_g[i % 2], g_host[i], bytes,
+                                    cudaMemcpyHostToDevice, cs));
+        TBJ_CUDA(h, launch_copy_ring(h->g, t->u, t->u_alt, cs));
+        h->launches += 1;
+        TBJ_CUDA(h, cudaEventRecord(h->hb_staged[i % 2], cs));
+        return JACOBI_OK;
+    };
+    if ((rc = stage(0))) return rc;
     long long total = 0, status = 0;
     for (int i = 0; i < count; ++i) {
-        // Take problem i's inputs: u0 into u (and u_alt, whose Dirichlet ring
-        // must equal u's), g into the buffer the solve reads.
-        TBJ_CUDA(h, cudaStreamWaitEvent(h->stream, h->hb_staged, 0));
-        TBJ_CUDA(h, cudaMemcpyAsync(h->u, h->hb_u, bytes, cudaMemcpyDeviceToDevice, h->stream));
-        TBJ_CUDA(h, cudaMemcpyAsync(h->u_alt, h->hb_u, bytes, cudaMemcpyDeviceToDevice, h->stream));
-        TBJ_CUDA(h, cudaMemcpyAsync(h->hb_gdev, h->hb_g, bytes, cudaMemcpyDeviceToDevice, h->stream));
-        TBJ_CUDA(h, cudaEventRecord(h->hb_taken, h->stream));
-        h->cur = 0;
-        // Stage problem i + 1's inputs while problem i is solved.
-        if (i + 1 < count) {
-            TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_taken, 0));
-            TBJ_CUDA(h, cudaMemcpyAsync(h->hb_u, u0_host[i + 1], bytes,
-                                        cudaMemcpyHostToDevice, cs));
-            TBJ_CUDA(h, cudaMemcpyAsync(h->hb_g, g_host[i + 1], bytes,
-                                        cudaMemcpyHostToDevice, cs));
-            TBJ_CUDA(h, cudaEventRecord(h->hb_staged, cs));
-        }
-        const long long k = jacobi_run(h, h->hb_gdev, steps,
+        jacobi_handle_t *t = hs[i % 2];
+        if (i + 1 < count && (rc = stage(i + 1))) return rc;
+        TBJ_CUDA(h, cudaStreamWaitEvent(h->stream, h->hb_staged[i % 2], 0));
+        t->cur = 0;
+        const long long before = t->launches;
+        const long long k = jacobi_run(t, h->hb_g[i % 2], steps,
                                        sweeps ? sweeps + (size_t)i * steps : nullptr);
+        if (t != h) h->launches += t->launches - before;
         if (k < 0) {
-            status = k;
+            status = t == h ? k : fail(h, (int)k, "%s", jacobi_last_error(t));
             break;
         }
         total += k;
-        // Problem i's result: into the outgoing buffer once the previous
-        // result has left it, then to the host while problem i + 1 runs.
-        TBJ_CUDA(h, cudaStreamWaitEvent(h->stream, h->hb_copied, 0));
-        TBJ_CUDA(h, cudaMemcpyAsync(h->hb_out, h->u, bytes, cudaMemcpyDeviceToDevice, h->stream));
-        TBJ_CUDA(h, cudaEventRecord(h->hb_result, h->stream));
-        TBJ_CUDA(h, cudaStreamWaitEvent(cs, h->hb_result, 0));
-        TBJ_CUDA(h, cudaMemcpyAsync(u_host[i], h->hb_out, bytes, cudaMemcpyDeviceToHost, cs));
-        TBJ_CUDA(h, cudaEventRecord(h->hb_copied, cs));
+        // jacobi_run returned with the stream idle: problem i's result is in
+        // t->u; it leaves on the copy stream while problem i + 1 runs.
+        TBJ_CUDA(h, cudaMemcpyAsync(u_host[i], t->u, bytes, cudaMemcpyDeviceToHost, cs));
     }
     TBJ_CUDA(h, cudaStreamSynchronize(cs));
+    // As documented: u holds the last problem's result (u_alt its ring).
+    const int last = status ? -1 : count - 1;
+    if (last >= 0 && hs[last % 2] != h) {
+        TBJ_CUDA(h, cudaMemcpyAsync(h->u, h->hb_tu, bytes, cudaMemcpyDeviceToDevice,
+                                    h->stream));
+        TBJ_CUDA(h, launch_copy_ring(h->g, h->u, h->u_alt, h->stream));
+        h->launches += 1;
+        h->cur = 0;
+    }
     TBJ_CUDA(h, cudaStreamSynchronize(h->stream));
     return status ? status : total;
 }

@@ -535,6 +535,9 @@ cudaError_t launch_rhs(const GridDesc &g, const float *u, const float *src,
                        float *b, cudaStream_t stream);
 cudaError_t launch_copy_interior(const GridDesc &g, const float *src,
                                  float *dst, cudaStream_t stream);
+// The Dirichlet ring (rows 0 and n-1, columns 0 and n-1) of src into dst.
+cudaError_t launch_copy_ring(const GridDesc &g, const float *src, float *dst,
+                             cudaStream_t stream);
 // Bounds-checked build only: NaN into dst's interior unless *stop is set
 // (stop may be null).
 cudaError_t launch_poison_interior(const GridDesc &g, float *dst,

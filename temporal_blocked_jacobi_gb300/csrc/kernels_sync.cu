@@ -342,6 +342,20 @@ __global__ void k_rhs(const float *__restrict__ u, const float *__restrict__ g,
     }
 }
 
+// The Dirichlet ring of src into dst: rows 0 and n-1, columns 0 and n-1.
+__global__ void k_copy_ring(const float *__restrict__ src, float *__restrict__ dst,
+                            int n, long long ld) {
+    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < 4 * n;
+         idx += gridDim.x * blockDim.x) {
+        const int side = idx / n, pos = idx % n;
+        const long long p = side == 0   ? (long long)pos
+                            : side == 1 ? (long long)(n - 1) * ld + pos
+                            : side == 2 ? (long long)pos * ld
+                                        : (long long)pos * ld + (n - 1);
+        dst[p] = src[p];
+    }
+}
+
 __global__ void k_copy_interior(const float *__restrict__ src,
                                 float *__restrict__ dst, int n, long long ld) {
     const int x0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -480,6 +494,13 @@ cudaError_t launch_poison_interior(const GridDesc &g, float *dst,
 cudaError_t launch_bounds_selftest(float *grid, int n, long long ld,
                                    unsigned *flags, cudaStream_t stream) {
     k_bounds_selftest<<<1, 32, 256, stream>>>(grid, n, ld, flags);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_ring(const GridDesc &g, const float *src, float *dst,
+                             cudaStream_t stream) {
+    const int blocks = (4 * g.n + 255) / 256 < 152 ? (4 * g.n + 255) / 256 : 152;
+    k_copy_ring<<<blocks, 256, 0, stream>>>(src, dst, g.n, g.ld);
     return cudaGetLastError();
 }
 

@@ -269,7 +269,9 @@ def test_run_host_matches_the_oracle_problem_by_problem():
     """jacobi_run_host: independent problems given as host buffers, each
     equal to the oracle's ten-step solve of its own inputs (different
     sources and boundary rows), whatever the copies' overlap; pinned and
-    pageable host memory."""
+    pageable host memory; odd and even problem counts (odd problems run on
+    the handle's second pair of fields), after which u holds the last
+    problem's result; and a second call after a change of strategy."""
     import torch
     from temporal_blocked_jacobi_gb300 import jacobi
     n, r, steps = 130, 10.0, 3
@@ -280,19 +282,29 @@ def test_run_host_matches_the_oracle_problem_by_problem():
         u0 = P.initial_field(n, ld, top=top)
         g = P.source_term(n, ld, src, amplitude=1000.0 * (k + 1) if src == "point" else None)
         cases.append((u0, g, *oracle.run(u0, g, r, steps=steps)[:2]))
+    def check(s, sel, pinned, kw):
+        u0s = [torch.from_numpy(cases[i][0]) for i in sel]
+        gs = [torch.from_numpy(cases[i][1]) for i in sel]
+        outs = [torch.full((n, ld), float("nan")) for _ in sel]
+        if pinned:
+            u0s = [t.pin_memory() for t in u0s]
+            gs = [t.pin_memory() for t in gs]
+            outs = [t.pin_memory() for t in outs]
+        counts = s.run_host(u0s, gs, outs, steps)
+        for i, got, k in zip(sel, outs, counts):
+            ref_u, ref_k = cases[i][2], cases[i][3]
+            assert k == ref_k, (kw, pinned, k, ref_k)
+            assert same_bits(got.numpy()[:, :n], ref_u[:, :n]), (kw, pinned, mismatch(got.numpy(), ref_u))
+        torch.cuda.synchronize()
+        assert same_bits(s.u.cpu().numpy()[:, :n], cases[sel[-1]][2][:, :n]), (kw, pinned)
+
     for pinned in (True, False):
         for kw in ({"strategy": "etb", "depth": 8, "control": "device"},
+                   {"strategy": "etb", "depth": 8, "tile": (112, 0), "control": "device"},
                    {"strategy": "sync", "control": "host"}):
             u, u_alt, b = jacobi.allocate(n, ld)
-            u0s = [torch.from_numpy(c[0]) for c in cases]
-            gs = [torch.from_numpy(c[1]) for c in cases]
-            outs = [torch.full((n, ld), float("nan")) for _ in cases]
-            if pinned:
-                u0s = [t.pin_memory() for t in u0s]
-                gs = [t.pin_memory() for t in gs]
-                outs = [t.pin_memory() for t in outs]
             with jacobi.Solver(u, u_alt, b, r, **kw) as s:
-                counts = s.run_host(u0s, gs, outs, steps)
-            for (u0, g, ref_u, ref_k), got, k in zip(cases, outs, counts):
-                assert k == ref_k, (kw, pinned, k, ref_k)
-                assert same_bits(got.numpy()[:, :n], ref_u[:, :n]), (kw, pinned, mismatch(got.numpy(), ref_u))
+                check(s, [0, 1, 2, 3], pinned, kw)
+                check(s, [3, 0, 2], pinned, kw)
+                s.set_strategy("sync", 1, control="device")
+                check(s, [1, 2], pinned, kw)
