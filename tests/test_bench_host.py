@@ -165,3 +165,35 @@ def test_kernel_name_follows_the_resolved_tile():
     assert bench.kernel_name("etb8", (112, 0)).startswith("k_etbs")
     assert bench.kernel_name("etb8@112x0").startswith("k_etbs")
     assert bench.kernel_name("etb8", (112, 92)).startswith("k_etbr")
+
+
+def test_cpu_baseline_times_the_whole_solve_when_it_is_small(monkeypatch):
+    """cpu_baseline runs the oracle's whole ten-step solve when the solve
+    needs at most FULL_SOLVE_LUPS lattice updates, and otherwise a sample of
+    about 1e10; the oracle itself is replaced by a recorder here."""
+    import types
+    calls = []
+
+    class FakeSample:
+        def __init__(self, n, r, source, threads=1):
+            self.n, self.threads = n, threads
+
+        def __call__(self, sweeps):
+            calls.append((self.n, self.threads, sweeps))
+            return 1.0, 2.0, sweeps
+
+    monkeypatch.setattr(bench, "OracleSample", FakeSample)
+    args = types.SimpleNamespace(workload="n2048_r10_gauss", cpu_sample_sweeps=0)
+    rec = bench.cpu_baseline(args, 4064)  # 4064 * 2046^2 = 1.7e10 updates
+    assert [c[2] for c in calls] == [4064, 4064]
+    assert rec["time_to_solution_s"] == 2.0 and "whole ten-step solve" in rec["sample"]
+    assert rec["cores"] == 1 and rec["all_cores"]["cores"] >= 1
+    calls.clear()
+    args = types.SimpleNamespace(workload="n18432_r10_point", cpu_sample_sweeps=0)
+    rec = bench.cpu_baseline(args, 2256)  # 7.7e11 updates: a sample
+    sweeps = calls[0][2]
+    assert sweeps % 8 == 0 and 0.5e10 <= sweeps * 18430 ** 2 <= 2e10
+    assert rec["time_to_solution_s"] is None and rec["sample"].startswith("first")
+    calls.clear()
+    bench.cpu_baseline(args, None)  # no GPU sweep count: a sample
+    assert calls[0][2] == sweeps
